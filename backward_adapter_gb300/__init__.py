@@ -1,0 +1,8 @@
+"""GB300-native fused flash-attention training op (forward + backward).
+
+The compute path is the C-ABI library libfa_train.so (hand-written sm_103a
+CUDA kernels); this package holds its build script, the ctypes binding and
+the seeded synthetic workloads used by tests and the benchmark.
+"""
+from .fa_train import (FaError, FaParams, bwd, bwd_accum, bwd_workspace_size, fwd,  # noqa: F401
+                       fwd_workspace_size, load_library, make_params)

@@ -1,0 +1,284 @@
+// C-ABI layer of the fused attention training op: parameter validation,
+// workspace planning and dispatch to the kernels. Nothing here allocates,
+// frees or synchronises; every launch goes on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/fa_train.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+constexpr int kMaxSeq = 1 << 24;
+
+fa_status check_params(const fa_params* p, Shape& s) {
+  g_last_error[0] = '\0';
+  if (p == nullptr) { set_error("params is NULL"); return FA_ERR_INVALID_ARG; }
+  if (p->B < 1 || p->B > 65535) { set_error("B=%d outside [1, 65535]", p->B); return FA_ERR_INVALID_ARG; }
+  if (p->Hkv < 1 || p->Hq < 1 || p->Hq > 65535) {
+    set_error("Hq=%d, Hkv=%d: need 1 <= Hkv, 1 <= Hq <= 65535", p->Hq, p->Hkv); return FA_ERR_INVALID_ARG;
+  }
+  if (p->Hq % p->Hkv != 0) { set_error("Hq=%d is not a multiple of Hkv=%d", p->Hq, p->Hkv); return FA_ERR_INVALID_ARG; }
+  if (p->Sq < 0 || p->Sq > kMaxSeq) { set_error("Sq=%d outside [0, %d]", p->Sq, kMaxSeq); return FA_ERR_INVALID_ARG; }
+  if (p->Sk < 1 || p->Sk > kMaxSeq) { set_error("Sk=%d outside [1, %d]", p->Sk, kMaxSeq); return FA_ERR_INVALID_ARG; }
+  if (p->D <= 0) { set_error("D=%d must be positive", p->D); return FA_ERR_INVALID_ARG; }
+  if (p->D != 64 && p->D != 128) { set_error("D=%d unsupported (64 or 128)", p->D); return FA_ERR_UNSUPPORTED; }
+  if (p->dtype != FA_F32 && p->dtype != FA_BF16) { set_error("dtype=%d invalid", p->dtype); return FA_ERR_INVALID_ARG; }
+  if (!std::isfinite(p->scale)) { set_error("scale is not finite"); return FA_ERR_INVALID_ARG; }
+  if (p->causal != 0 && p->causal != 1) { set_error("causal=%d must be 0 or 1", p->causal); return FA_ERR_INVALID_ARG; }
+  if (p->mask_kind < FA_MASK_NONE || p->mask_kind > FA_MASK_BOOL_U8) {
+    set_error("mask_kind=%d invalid", p->mask_kind); return FA_ERR_INVALID_ARG;
+  }
+  if (p->mask_kind != FA_MASK_NONE && p->mask_batch != 1 && p->mask_batch != p->B) {
+    set_error("mask_batch=%d must be 1 or B=%d", p->mask_batch, p->B); return FA_ERR_INVALID_ARG;
+  }
+  if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
+  if (p->causal && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
+    set_error("causal q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
+              (long long)p->q_offset, p->Sq, p->Sk);
+    return FA_ERR_INVALID_ARG;
+  }
+  s.B = p->B; s.Hq = p->Hq; s.Hkv = p->Hkv; s.Sq = p->Sq; s.Sk = p->Sk; s.D = p->D;
+  s.dtype = p->dtype; s.scale = p->scale; s.causal = p->causal; s.mask_kind = p->mask_kind;
+  s.mask_batch = p->mask_kind == FA_MASK_NONE ? 1 : p->mask_batch;
+  s.q_offset = p->causal ? (long long)p->q_offset : 0;
+  return FA_OK;
+}
+
+size_t elem_size(const Shape& s) { return s.dtype == DT_BF16 ? 2 : 4; }
+size_t q_bytes(const Shape& s) { return (size_t)s.B * s.Hq * s.Sq * s.D * elem_size(s); }
+size_t kv_bytes(const Shape& s, size_t es) { return (size_t)s.B * s.Hkv * s.Sk * s.D * es; }
+size_t mask_bytes(const Shape& s) {
+  if (s.mask_kind == MK_NONE) return 0;
+  return (size_t)s.mask_batch * s.Sq * s.Sk * (s.mask_kind == MK_ADD ? 4 : 1);
+}
+
+struct Span { const void* p; size_t n; const char* name; };
+
+bool overlaps(const Span& a, const Span& b) {
+  if (a.p == nullptr || b.p == nullptr || a.n == 0 || b.n == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+  return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+fa_status check_buffers(const Span* in, int nin, const Span* out, int nout) {
+  for (int i = 0; i < nin + nout; ++i) {
+    const Span& x = i < nin ? in[i] : out[i - nin];
+    if (x.n == 0) continue;
+    if (x.p == nullptr) { set_error("%s is NULL", x.name); return FA_ERR_INVALID_ARG; }
+    if ((uintptr_t)x.p % 16 != 0) { set_error("%s is not 16-byte aligned", x.name); return FA_ERR_INVALID_ARG; }
+  }
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(out[o], in[i])) { set_error("output %s overlaps input %s", out[o].name, in[i].name); return FA_ERR_INVALID_ARG; }
+    for (int o2 = o + 1; o2 < nout; ++o2)
+      if (overlaps(out[o], out[o2])) { set_error("outputs %s and %s overlap", out[o].name, out[o2].name); return FA_ERR_INVALID_ARG; }
+  }
+  return FA_OK;
+}
+
+fa_status check_ws(void* ws, size_t ws_bytes, size_t need, const Span* bufs, int n) {
+  if (ws_bytes < need) { set_error("workspace %zu bytes < %zu needed", ws_bytes, need); return FA_ERR_WORKSPACE; }
+  if (need == 0) return FA_OK;
+  if (ws == nullptr) { set_error("workspace is NULL"); return FA_ERR_WORKSPACE; }
+  if ((uintptr_t)ws % kAlign != 0) { set_error("workspace is not %zu-byte aligned", kAlign); return FA_ERR_INVALID_ARG; }
+  const Span w{ws, need, "workspace"};
+  for (int i = 0; i < n; ++i)
+    if (overlaps(w, bufs[i])) { set_error("workspace overlaps %s", bufs[i].name); return FA_ERR_INVALID_ARG; }
+  return FA_OK;
+}
+
+fa_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FA_OK;
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return FA_ERR_CUDA;
+}
+
+// The tcgen05 path takes bf16 inputs; fp32 inputs stay on the SIMT fp32 path.
+bool use_tensor_cores(const Shape& s) { return s.dtype == DT_BF16 && tc_supported(s); }
+
+thread_local cudaEvent_t g_prof_start[KID_COUNT] = {};
+thread_local cudaEvent_t g_prof_stop[KID_COUNT] = {};
+thread_local uint64_t g_launches = 0;
+
+}  // namespace
+
+cudaError_t prof_begin(int kid, cudaStream_t st) {
+  return g_prof_start[kid] ? cudaEventRecord(g_prof_start[kid], st) : cudaSuccess;
+}
+cudaError_t prof_end(int kid, cudaStream_t st) {
+  return g_prof_stop[kid] ? cudaEventRecord(g_prof_stop[kid], st) : cudaSuccess;
+}
+void count_launches(int n) { g_launches += (uint64_t)n; }
+
+FwdPlan plan_fwd(const Shape& s) {
+  FwdPlan p{};
+  p.tensor_core = use_tensor_cores(s);
+  p.kv_splits = p.tensor_core ? tc_fwd_kv_splits(s) : 1;
+  size_t off = 0;
+  if (p.tensor_core && s.mask_kind != MK_NONE) {
+    p.tilemap_off = off;
+    p.tilemap_bytes = (size_t)s.mask_batch * ((s.Sq + 127) / 128) * ((s.Sk + 127) / 128);
+    off = align_up(off + p.tilemap_bytes);
+  }
+  if (p.kv_splits > 1) {
+    const size_t rows = (size_t)s.B * s.Hq * s.Sq;
+    p.part_o_off = off;
+    p.part_o_bytes = (size_t)p.kv_splits * rows * s.D * 4;
+    off = align_up(off + p.part_o_bytes);
+    p.part_ml_off = off;
+    p.part_ml_bytes = (size_t)p.kv_splits * rows * 2 * 4;
+    off = align_up(off + p.part_ml_bytes);
+  }
+  p.total = off;
+  return p;
+}
+
+BwdPlan plan_bwd(const Shape& s) {
+  BwdPlan p{};
+  p.tensor_core = use_tensor_cores(s);
+  size_t off = 0;
+  const size_t rows = (size_t)s.B * s.Hq * s.Sq;
+  if (p.tensor_core && s.mask_kind != MK_NONE) {
+    p.tilemap_off = off;
+    p.tilemap_bytes = (size_t)s.mask_batch * ((s.Sq + 127) / 128) * ((s.Sk + 127) / 128);
+    off = align_up(off + p.tilemap_bytes);
+  }
+  p.dsum_off = off;
+  p.dsum_bytes = rows * 4;
+  off = align_up(off + p.dsum_bytes);
+  if (p.tensor_core) {
+    p.dqacc_off = off;
+    p.dqacc_bytes = rows * s.D * 4;
+    off = align_up(off + p.dqacc_bytes);
+  }
+  p.total = off;
+  return p;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+size_t fa_train_fwd_workspace_size(const fa_params* p) {
+  Shape s;
+  if (check_params(p, s) != FA_OK) return 0;
+  return plan_fwd(s).total;
+}
+
+size_t fa_train_bwd_workspace_size(const fa_params* p) {
+  Shape s;
+  if (check_params(p, s) != FA_OK) return 0;
+  return plan_bwd(s).total;
+}
+
+fa_status fa_train_fwd(const fa_params* p, const void* q, const void* k, const void* v, const void* mask, void* o,
+                       float* lse, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  fa_status st = check_params(p, s);
+  if (st != FA_OK) return st;
+  const size_t es = elem_size(s);
+  const Span in[] = {{q, q_bytes(s), "q"}, {k, kv_bytes(s, es), "k"}, {v, kv_bytes(s, es), "v"},
+                     {mask, mask_bytes(s), "mask"}};
+  const Span out[] = {{o, q_bytes(s), "o"}, {lse, (size_t)s.B * s.Hq * s.Sq * 4, "lse"}};
+  if ((st = check_buffers(in, 4, out, 2)) != FA_OK) return st;
+  const FwdPlan plan = plan_fwd(s);
+  const Span all[] = {in[0], in[1], in[2], in[3], out[0], out[1]};
+  if ((st = check_ws(ws, ws_bytes, plan.total, all, 6)) != FA_OK) return st;
+  if (s.Sq == 0) return FA_OK;
+
+  FwdArgs a{s, q, k, v, mask, o, lse, (cudaStream_t)stream};
+  cudaError_t e = plan.tensor_core ? tc_fwd(a, plan, (char*)ws) : simt_fwd(a);
+  return cuda_status(e, "forward launch");
+}
+
+static fa_status bwd_common(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
+                            const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            bool accum, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  fa_status st = check_params(p, s);
+  if (st != FA_OK) return st;
+  const size_t es = elem_size(s);
+  const size_t rows = (size_t)s.B * s.Hq * s.Sq;
+  const Span in[] = {{q, q_bytes(s), "q"}, {k, kv_bytes(s, es), "k"}, {v, kv_bytes(s, es), "v"},
+                     {mask, mask_bytes(s), "mask"}, {o, q_bytes(s), "o"}, {lse, rows * 4, "lse"},
+                     {dO, q_bytes(s), "dO"}};
+  const size_t gk = accum ? kv_bytes(s, 4) : kv_bytes(s, es);
+  const Span out[] = {{dq, q_bytes(s), "dq"}, {dk, gk, accum ? "dk_acc" : "dk"}, {dv, gk, accum ? "dv_acc" : "dv"}};
+  if ((st = check_buffers(in, 7, out, 3)) != FA_OK) return st;
+  const BwdPlan plan = plan_bwd(s);
+  const Span all[] = {in[0], in[1], in[2], in[3], in[4], in[5], in[6], out[0], out[1], out[2]};
+  if ((st = check_ws(ws, ws_bytes, plan.total, all, 10)) != FA_OK) return st;
+
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (s.Sq == 0) {
+    // No query rows: the gradient of every key is zero.
+    if (accum) return FA_OK;
+    cudaError_t e = cudaMemsetAsync(dk, 0, gk, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, gk, cs);
+    return cuda_status(e, "zero dK/dV");
+  }
+  BwdArgs a{s, q, k, v, mask, o, lse, dO, dq, dk, dv, accum, cs};
+  cudaError_t e = plan.tensor_core ? tc_bwd(a, plan, (char*)ws)
+                                   : simt_bwd(a, reinterpret_cast<float*>((char*)ws + plan.dsum_off));
+  return cuda_status(e, "backward launch");
+}
+
+fa_status fa_train_bwd(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
+                       const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk, dv, false, ws, ws_bytes, stream);
+}
+
+fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
+                             const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
+                             float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
+  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream);
+}
+
+const char* fa_status_str(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_WORKSPACE: return "workspace too small";
+    case FA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char* fa_last_error(void) { return g_last_error; }
+
+fa_status fa_profile_set_events(int kernel, void* start_event, void* stop_event) {
+  if (kernel < 0 || kernel >= KID_COUNT) {
+    set_error("unknown kernel id %d", kernel);
+    return FA_ERR_INVALID_ARG;
+  }
+  g_prof_start[kernel] = (cudaEvent_t)start_event;
+  g_prof_stop[kernel] = (cudaEvent_t)stop_event;
+  return FA_OK;
+}
+
+uint64_t fa_profile_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// HBM-bound helper passes of the fused attention training op:
+//   * D precompute: D_i = <dO_i, O_i> in fp32, fused with zeroing the fp32 dQ
+//     accumulator (llama.cpp PR #57, commit 86c140d: the tiled backward forms
+//     LSE and D before the per-tile gradients);
+//   * dQ convert: dQ = scale * dQ_acc, rounded to the output type;
+//   * mask tile classification: one byte per 128x128 tile saying whether the
+//     tile is fully hidden (skipped), fully open with zero bias (no mask reads
+//     in the hot loop) or mixed.
+// Each thread moves 16-byte vectors; rows are split across 8..16 lanes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// 8 consecutive elements as fp32, from a 16-byte (bf16) or 32-byte (fp32) vector.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 f = __bfloat1622float2(h[t]);
+    x[2 * t] = f.x;
+    x[2 * t + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* x) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* x) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) h[t] = __floats2bfloat162_rn(x[2 * t], x[2 * t + 1]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float* x) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, const T* __restrict__ dO,
+                                                   float* __restrict__ dsum, float* __restrict__ dq_acc,
+                                                   long long rows) {
+  constexpr int LPR = D / 8;  // lanes per row
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = tid / LPR;
+  const int part = (int)(tid % LPR);
+  float acc = 0.f;
+  if (row < rows) {
+    float a[8], g[8];
+    load8(o + row * D + part * 8, a);
+    load8(dO + row * D + part * 8, g);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc = fmaf(a[t], g[t], acc);
+    if (dq_acc != nullptr) {
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      store8(dq_acc + row * D + part * 8, z);
+    }
+  }
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) dsum[row] = acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
+                                                         float scale, long long vecs) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= vecs) return;
+  float x[8];
+  load8(acc + i * 8, x);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) x[t] *= scale;
+  store8(dq + i * 8, x);
+}
+
+// One block per (mask batch, q-tile, k-tile) of 128 x 128.
+__global__ void __launch_bounds__(256) mask_classify_kernel(Shape s, const void* __restrict__ mask,
+                                                            uint8_t* __restrict__ tilemap) {
+  const int kt = blockIdx.x, qt = blockIdx.y, mb = blockIdx.z;
+  const int nqt = gridDim.y, nkt = gridDim.x;
+  bool any_vis = false, all_open = true;
+  for (int e = threadIdx.x; e < 128 * 128; e += 256) {
+    const int i = qt * 128 + e / 128, j = kt * 128 + e % 128;
+    if (i >= s.Sq || j >= s.Sk) continue;
+    const size_t idx = ((size_t)mb * s.Sq + i) * s.Sk + j;
+    if (s.mask_kind == MK_ADD) {
+      const float m = static_cast<const float*>(mask)[idx];
+      const bool vis = m > kMaskFloor;
+      any_vis |= vis;
+      all_open &= (m == 0.f);
+    } else {
+      const bool vis = static_cast<const uint8_t*>(mask)[idx] != 0;
+      any_vis |= vis;
+      all_open &= vis;
+    }
+  }
+  any_vis = __syncthreads_or(any_vis);
+  all_open = __syncthreads_and(all_open);
+  if (threadIdx.x == 0)
+    tilemap[((size_t)mb * nqt + qt) * nkt + kt] = !any_vis ? TILE_SKIP : (all_open ? TILE_OPEN : TILE_MIXED);
+}
+
+}  // namespace
+
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero) {
+  const Shape& s = a.s;
+  const long long rows = (long long)s.B * s.Hq * s.Sq;
+  if (rows == 0) return cudaSuccess;
+  const long long threads = rows * (s.D / 8);
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  cudaError_t e = prof_begin(KID_BWD_DSUM, a.stream);
+  if (e != cudaSuccess) return e;
+  if (s.dtype == DT_BF16) {
+    if (s.D == 64)
+      dsum_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows);
+    else
+      dsum_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows);
+  } else {
+    if (s.D == 64)
+      dsum_kernel<float, 64><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
+                                                           dq_acc_to_zero, rows);
+    else
+      dsum_kernel<float, 128><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
+                                                            dq_acc_to_zero, rows);
+  }
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return prof_end(KID_BWD_DSUM, a.stream);
+}
+
+cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc) {
+  const Shape& s = a.s;
+  const long long vecs = (long long)s.B * s.Hq * s.Sq * s.D / 8;
+  if (vecs == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((vecs + 255) / 256);
+  cudaError_t e = prof_begin(KID_BWD_DQCONV, a.stream);
+  if (e != cudaSuccess) return e;
+  if (s.dtype == DT_BF16)
+    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(dq_acc, (__nv_bfloat16*)a.dq, s.scale, vecs);
+  else
+    dq_convert_kernel<float><<<blocks, 256, 0, a.stream>>>(dq_acc, (float*)a.dq, s.scale, vecs);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return prof_end(KID_BWD_DQCONV, a.stream);
+}
+
+cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st) {
+  if (s.mask_kind == MK_NONE || s.Sq == 0) return cudaSuccess;
+  dim3 grid((s.Sk + 127) / 128, (s.Sq + 127) / 128, s.mask_batch);
+  cudaError_t e = prof_begin(KID_MASK, st);
+  if (e != cudaSuccess) return e;
+  mask_classify_kernel<<<grid, 256, 0, st>>>(s, mask, tilemap);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return prof_end(KID_MASK, st);
+}
+
+}  // namespace fa

@@ -1,0 +1,96 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+enum : int { DT_F32 = 0, DT_BF16 = 1 };
+enum : int { MK_NONE = 0, MK_ADD = 1, MK_BOOL = 2 };
+
+// Tile-map codes produced by the mask classifier (one byte per 128x128 tile).
+enum : uint8_t { TILE_SKIP = 0, TILE_OPEN = 1, TILE_MIXED = 2 };
+
+struct Shape {
+  int B, Hq, Hkv, Sq, Sk, D;
+  int dtype;
+  float scale;
+  int causal;
+  int mask_kind;
+  int mask_batch;
+  long long q_offset;
+};
+
+struct FwdArgs {
+  Shape s;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* mask;
+  void* o;
+  float* lse;
+  cudaStream_t stream;
+};
+
+struct BwdArgs {
+  Shape s;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* mask;
+  const void* o;
+  const float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;  // dtype when !accum, fp32 accumulator when accum
+  void* dv;
+  bool accum;
+  cudaStream_t stream;
+};
+
+// Carve-up of the caller's workspace. Offsets are 256-byte aligned.
+struct FwdPlan {
+  bool tensor_core;   // tcgen05 path (bf16) vs SIMT fp32 path
+  int kv_splits;      // > 1: split-KV partials + combine
+  size_t tilemap_off, tilemap_bytes;
+  size_t part_o_off, part_o_bytes;     // fp32 [splits, B, Hq, Sq, D]
+  size_t part_ml_off, part_ml_bytes;   // fp32 [splits, B, Hq, Sq, 2]
+  size_t total;
+};
+
+struct BwdPlan {
+  bool tensor_core;
+  size_t tilemap_off, tilemap_bytes;
+  size_t dsum_off, dsum_bytes;   // fp32 [B, Hq, Sq]
+  size_t dqacc_off, dqacc_bytes; // fp32 [B, Hq, Sq, D]
+  size_t total;
+};
+
+// Tracing hooks (fa_profile_set_events): per-thread events recorded around a
+// kernel family, and a per-thread launch counter.
+enum : int { KID_FWD = 0, KID_BWD_MAIN = 1, KID_BWD_DSUM = 2, KID_BWD_DQCONV = 3, KID_MASK = 4, KID_COUNT = 5 };
+cudaError_t prof_begin(int kid, cudaStream_t st);
+cudaError_t prof_end(int kid, cudaStream_t st);
+void count_launches(int n);
+
+FwdPlan plan_fwd(const Shape& s);
+BwdPlan plan_bwd(const Shape& s);
+
+// SIMT fp32 kernels (any dtype, D in {64, 128}).
+cudaError_t simt_fwd(const FwdArgs& a);
+cudaError_t simt_bwd(const BwdArgs& a, float* dsum);
+
+// Helper passes shared by both paths.
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero);
+cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc);
+cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
+
+// tcgen05 paths (bf16, D in {64, 128}).
+bool tc_supported(const Shape& s);
+int tc_fwd_kv_splits(const Shape& s);
+cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);
+cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws);
+
+}  // namespace fa

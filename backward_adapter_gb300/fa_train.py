@@ -1,0 +1,222 @@
+"""Thin Python binding of the C-ABI library libfa_train.so (include/fa_train.h).
+
+Argument marshalling only: PyTorch supplies device memory and the current
+CUDA stream, ctypes passes raw pointers and sizes, and every step of the op
+runs in the library's CUDA kernels. There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_train.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA = range(5)
+FA_F32, FA_BF16 = 0, 1
+FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
+
+EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
+            "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
+            "fa_profile_launch_count")
+FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
+
+
+class FaParams(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("mask_kind", ctypes.c_int32), ("mask_batch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("q_offset", ctypes.c_int64)]
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"fa_train: {_status_name(status)} ({status}): {detail}")
+        self.status = status
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfa_train.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with backward_adapter_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(FaParams)
+    vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    lib.fa_train_fwd_workspace_size.argtypes = [P]
+    lib.fa_train_fwd_workspace_size.restype = sz
+    lib.fa_train_bwd_workspace_size.argtypes = [P]
+    lib.fa_train_bwd_workspace_size.restype = sz
+    lib.fa_train_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_fwd.restype = st
+    lib.fa_train_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_bwd.restype = st
+    lib.fa_train_bwd_accum.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_bwd_accum.restype = st
+    lib.fa_status_str.argtypes = [st]
+    lib.fa_status_str.restype = ctypes.c_char_p
+    lib.fa_last_error.argtypes = []
+    lib.fa_last_error.restype = ctypes.c_char_p
+    lib.fa_profile_set_events.argtypes = [st, vp, vp]
+    lib.fa_profile_set_events.restype = st
+    lib.fa_profile_launch_count.argtypes = []
+    lib.fa_profile_launch_count.restype = ctypes.c_uint64
+    _lib = lib
+    return lib
+
+
+def _status_name(s: int) -> str:
+    try:
+        return load_library().fa_status_str(s).decode()
+    except Exception:  # library not loadable while formatting an error
+        return str(s)
+
+
+def _check(status: int) -> None:
+    if status != FA_OK:
+        raise FaError(status, load_library().fa_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _mask_view(mask: Optional[torch.Tensor]):
+    if mask is None:
+        return None, FA_MASK_NONE, 1
+    if mask.dim() != 3:
+        raise ValueError("mask must be [mask_batch, Sq, Sk]")
+    if mask.dtype == torch.float32:
+        return mask, FA_MASK_ADD_F32, mask.shape[0]
+    if mask.dtype == torch.bool:
+        return mask.view(torch.uint8), FA_MASK_BOOL_U8, mask.shape[0]
+    if mask.dtype == torch.uint8:
+        return mask, FA_MASK_BOOL_U8, mask.shape[0]
+    raise TypeError(f"mask dtype {mask.dtype}: float32 (additive) or uint8/bool (1 = attend)")
+
+
+def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] = None, *,
+                scale: Optional[float] = None, causal: bool = False,
+                q_offset: Optional[int] = None) -> FaParams:
+    """Fill fa_params from tensor shapes. q: [B,Hq,Sq,D], k: [B,Hkv,Sk,D]."""
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    _, kind, mb = _mask_view(mask)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if q_offset is None:
+        q_offset = Sk - Sq if causal else 0
+    return FaParams(B, Hq, Hkv, Sq, Sk, D, _dtype_code(q), float(scale), int(bool(causal)), kind, mb, 0,
+                    int(q_offset))
+
+
+def fwd_workspace_size(p: FaParams) -> int:
+    return int(load_library().fa_train_fwd_workspace_size(ctypes.byref(p)))
+
+
+def bwd_workspace_size(p: FaParams) -> int:
+    return int(load_library().fa_train_bwd_workspace_size(ctypes.byref(p)))
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return ws
+    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+        return ws
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
+
+
+def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, out=None, lse=None,
+        workspace=None, stream=None):
+    """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32)."""
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, k, v, mview)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    ws_bytes = fwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    _check(lib.fa_train_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(out), _ptr(lse),
+                            _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    return out, lse
+
+
+def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, dq=None, dk=None,
+        dv=None, workspace=None, stream=None):
+    """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers)."""
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, k, v, o, lse, do, mview)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = bwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    _check(lib.fa_train_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                            _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes,
+                            _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, causal=False, q_offset=None,
+              dq=None, workspace=None, stream=None):
+    """Accumulating backward: dK/dV are added into fp32 dk_acc/dv_acc in place; returns dQ."""
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
+    if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
+        raise TypeError("dk_acc and dv_acc must be float32")
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset)
+    dq = torch.empty_like(q) if dq is None else dq
+    ws_bytes = bwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    _check(lib.fa_train_bwd_accum(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                  _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
+                                  _stream(q.device, stream)))
+    return dq
+
+
+def profile_set_events(kernel: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event start/stop around a kernel family on later calls (None clears)."""
+    _check(load_library().fa_profile_set_events(kernel, None if start is None else start.cuda_event,
+                                                None if stop is None else stop.cuda_event))
+
+
+def profile_launch_count() -> int:
+    """Kernels the library has launched from this thread so far."""
+    return int(load_library().fa_profile_launch_count())

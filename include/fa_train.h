@@ -1,0 +1,169 @@
+/*
+ * fa_train.h — C ABI of the fused flash-attention training op for one GB300 (sm_103a).
+ *
+ * What the op computes (flash-attn-training skill, trap list items 5, 8 and 9;
+ * llama.cpp PR #57 "train: the exact walk at her real window", commit 86c140d
+ * "tiled flash-attention backward"):
+ *
+ *   forward   s_ij = scale * <q_i, k_j> + mask_ij ; P = softmax over the visible
+ *             keys of row i ; O_i = sum_j P_ij v_j ; LSE_i = ln sum_vis exp(s_ij).
+ *             A query row with no visible key gets O_i = 0 and LSE_i = 0.
+ *   backward  P is recomputed from LSE ; D_i = <dO_i, O_i> ;
+ *             dS_ij = P_ij (<dO_i, v_j> - D_i) ; dQ = scale dS K ;
+ *             dK = scale dS^T Q ; dV = P^T dO, with dK/dV summed over the query
+ *             heads that share a key/value head (native GQA, no head expansion).
+ *   accumulate variant: dK/dV are added into caller-owned fp32 buffers
+ *             (PR #57, commit 86c140d: a node's gradient is added into an
+ *             existing tensor instead of being returned).
+ *
+ * Conventions (the pages leave these open; these are the plain readings):
+ *   - Layout: every tensor is contiguous row-major. Q, O, dO, dQ: [B, Hq, Sq, D];
+ *     K, V, dK, dV: [B, Hkv, Sk, D]; LSE: [B, Hq, Sq] fp32; mask: [mask_batch, Sq, Sk].
+ *   - GQA: query head h reads key/value head h / (Hq / Hkv).
+ *   - Additive mask (FA_MASK_ADD_F32): a value <= -1e9 (or -inf) hides the pair
+ *     (its probability is exactly 0); any larger value is a bias added after scaling.
+ *   - Boolean mask (FA_MASK_BOOL_U8): 1 = attend, 0 = hidden.
+ *   - Causal: key j is visible to query i iff j <= q_offset + i (a query chunk
+ *     sitting at positions q_offset.. of a longer cached window). Mask and
+ *     causal combine (a pair must pass both).
+ *   - LSE is a natural logarithm. O, dQ, dK, dV have the input element type;
+ *     bf16 results are rounded to nearest even from fp32 accumulators.
+ *
+ * Ownership and execution:
+ *   - All data pointers are DEVICE pointers (CUDA global memory) owned by the caller.
+ *     The library never allocates, frees or synchronises; all work is enqueued on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream) and returns
+ *     before the GPU has finished.
+ *   - `ws` is caller-owned device scratch of at least the size the matching
+ *     *_workspace_size() query returns (ws may be NULL when that size is 0). Its
+ *     contents need no initialisation and are garbage afterwards. Two calls in
+ *     flight at once must not share a workspace.
+ *   - Outputs must not alias inputs or each other.
+ *
+ * Errors: parameters are validated before anything is enqueued. A rejected call
+ * returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE and leaves
+ * every buffer untouched. A failed launch returns FA_ERR_CUDA. fa_last_error()
+ * gives a one-line description of the most recent failure on the calling thread.
+ */
+#ifndef FA_TRAIN_H
+#define FA_TRAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* a shape, pointer, alignment or enum value is invalid */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D not in {64, 128}) */
+  FA_ERR_WORKSPACE = 3,   /* ws_bytes is smaller than the size query returns */
+  FA_ERR_CUDA = 4         /* a CUDA launch or runtime call failed */
+} fa_status;
+
+typedef enum fa_dtype { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum fa_mask_kind {
+  FA_MASK_NONE = 0,
+  FA_MASK_ADD_F32 = 1, /* float32 additive mask, <= -1e9 hides a pair */
+  FA_MASK_BOOL_U8 = 2  /* uint8 boolean mask, nonzero = attend */
+} fa_mask_kind;
+
+typedef struct fa_params {
+  int32_t B;          /* batch, >= 1 */
+  int32_t Hq;         /* query heads, a multiple of Hkv */
+  int32_t Hkv;        /* key/value heads, >= 1 */
+  int32_t Sq;         /* query rows per head, >= 0 (0 makes every call a no-op) */
+  int32_t Sk;         /* keys per head, >= 1 */
+  int32_t D;          /* head dimension: 64 or 128 */
+  int32_t dtype;      /* fa_dtype of Q, K, V, O, dO, dQ, dK, dV */
+  float scale;        /* softmax scale, finite */
+  int32_t causal;     /* 0 or 1 */
+  int32_t mask_kind;  /* fa_mask_kind */
+  int32_t mask_batch; /* 1 (broadcast over batch) or B; ignored without a mask */
+  int32_t reserved;   /* must be 0 */
+  int64_t q_offset;   /* causal only: key position of query row 0; needs 0 <= q_offset and q_offset + Sq <= Sk */
+} fa_params;
+
+/* Bytes of scratch the forward needs for these parameters (0 when none). */
+FA_API size_t fa_train_fwd_workspace_size(const fa_params* p);
+
+/* Bytes of scratch the backward (both variants) needs for these parameters. */
+FA_API size_t fa_train_bwd_workspace_size(const fa_params* p);
+
+/*
+ * Forward: writes O [B,Hq,Sq,D] (dtype) and LSE [B,Hq,Sq] (fp32).
+ * mask may be NULL only when p->mask_kind == FA_MASK_NONE.
+ * Every pointer must be 16-byte aligned.
+ */
+FA_API fa_status fa_train_fwd(const fa_params* p, const void* q, const void* k, const void* v,
+                       const void* mask, void* o, float* lse, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Backward: from Q, K, V, mask, the forward's O and LSE and the upstream
+ * gradient dO, writes (overwrites) dQ [B,Hq,Sq,D], dK and dV [B,Hkv,Sk,D], all
+ * in dtype. O and LSE must be the forward's outputs for the same inputs.
+ */
+FA_API fa_status fa_train_bwd(const fa_params* p, const void* q, const void* k, const void* v,
+                       const void* mask, const void* o, const float* lse, const void* dO,
+                       void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Accumulating backward: as fa_train_bwd, but dK and dV are ADDED into the
+ * caller's fp32 buffers dk_acc/dv_acc [B,Hkv,Sk,D] (fp32 sums, no bf16 rounding
+ * of the increment). dQ is overwritten in dtype. Rows of dk_acc/dv_acc whose key
+ * is visible to no query receive +0.
+ */
+FA_API fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const void* k, const void* v,
+                             const void* mask, const void* o, const float* lse, const void* dO,
+                             void* dq, float* dk_acc, float* dv_acc, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * Tracing (optional). Kernels of the op, as named for fa_profile_set_events.
+ * FA_KERNEL_FWD: the forward main kernel (plus the split-KV combine when used);
+ * FA_KERNEL_BWD_MAIN: the backward main kernel(s) that form dQ/dK/dV;
+ * FA_KERNEL_BWD_DSUM: the D = rowsum(dO*O) pass; FA_KERNEL_BWD_DQ_CONVERT: the
+ * fp32 -> dtype dQ pass; FA_KERNEL_MASK_CLASSIFY: the mask tile classifier.
+ */
+typedef enum fa_kernel_id {
+  FA_KERNEL_FWD = 0,
+  FA_KERNEL_BWD_MAIN = 1,
+  FA_KERNEL_BWD_DSUM = 2,
+  FA_KERNEL_BWD_DQ_CONVERT = 3,
+  FA_KERNEL_MASK_CLASSIFY = 4,
+  FA_KERNEL_COUNT = 5
+} fa_kernel_id;
+
+/*
+ * Make later calls on the calling thread record `start_event` just before and
+ * `stop_event` just after the given kernel(s), on the stream they launch on.
+ * Both are cudaEvent_t handles owned by the caller (NULL, NULL clears the hook).
+ * Returns FA_ERR_INVALID_ARG for an unknown kernel id. Recording errors are
+ * reported by the op call that records them (FA_ERR_CUDA).
+ */
+FA_API fa_status fa_profile_set_events(int kernel, void* start_event, void* stop_event);
+
+/* Number of CUDA kernels the library has launched from the calling thread so far. */
+FA_API uint64_t fa_profile_launch_count(void);
+
+/* Static description of a status code. */
+FA_API const char* fa_status_str(fa_status s);
+
+/* One-line description of the most recent failure on the calling thread ("" if none). */
+FA_API const char* fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_TRAIN_H */

@@ -1,0 +1,95 @@
+"""Helpers for the GPU parity tests: run the CUDA path (through the C-ABI
+binding) and the fp64 oracle on the same seeded inputs and compare them."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from backward_adapter_gb300 import fa_train as ft
+from backward_adapter_gb300 import workloads as wl
+from oracle import attention as ref
+
+# Tolerances: bf16 inputs with fp32 accumulation vs fp32 inputs.
+TOL = {"bf16": (1e-2, 1e-3), "f32": (1e-4, 0.0)}
+LSE_ABS = 1e-3
+
+
+def torch_dtype(w: wl.Workload):
+    return torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+
+def to_device(inputs: dict, w: wl.Workload, device="cuda"):
+    dt = torch_dtype(w)
+    t = {n: torch.from_numpy(inputs[n]).to(device).to(dt).contiguous() for n in ("q", "k", "v", "do")}
+    m = inputs["mask"]
+    t["mask"] = None if m is None else torch.from_numpy(m).to(device).contiguous()
+    if w.accum:
+        t["dk_acc"] = torch.from_numpy(inputs["dk_acc"]).to(device).contiguous()
+        t["dv_acc"] = torch.from_numpy(inputs["dv_acc"]).to(device).contiguous()
+    return t
+
+
+def run_gpu(w: wl.Workload, t: dict) -> dict:
+    """Forward + backward on the GPU; returns float64 numpy copies of every output."""
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
+    o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
+    if w.accum:
+        dk, dv = t["dk_acc"].clone(), t["dv_acc"].clone()
+        dq = ft.bwd_accum(t["q"], t["k"], t["v"], o, lse, t["do"], dk, dv, t["mask"], **kw)
+    else:
+        dq, dk, dv = ft.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], t["mask"], **kw)
+    torch.cuda.synchronize()
+    return {n: x.double().cpu().numpy() for n, x in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def run_oracle(w: wl.Workload, inputs: dict, q_heads=None, kv_heads=None) -> dict:
+    """Oracle on all heads, or on the given query heads and the key/value heads they read."""
+    q, k, v, do = inputs["q"], inputs["k"], inputs["v"], inputs["do"]
+    if q_heads is not None:
+        q, do = q[:, q_heads], do[:, q_heads]
+        k, v = k[:, kv_heads], v[:, kv_heads]
+    args = (q, k, v, do)
+    kw = dict(mask=inputs["mask"], mask_kind=inputs["mask_kind"], causal=w.causal, q_offset=w.q_offset)
+    if w.accum:
+        dka, dva = inputs["dk_acc"], inputs["dv_acc"]
+        if kv_heads is not None:
+            dka, dva = dka[:, kv_heads], dva[:, kv_heads]
+        return ref.backward_accumulate(*args, dka, dva, w.scale, **kw)
+    return ref.backward(*args, w.scale, **kw)
+
+
+def max_err(got, exp):
+    return float(np.abs(got - exp).max()) if got.size else 0.0
+
+
+def assert_parity(w: wl.Workload, got: dict, exp: dict, where: str = ""):
+    rel, abs_ = TOL[w.dtype]
+    for n in ("o", "dq", "dk", "dv"):
+        e = max_err(got[n], exp[n])
+        bound = rel * float(np.abs(exp[n]).max()) + abs_
+        assert e <= bound, f"{w.name}{where}: {n} max-abs err {e:.3e} > {bound:.3e}"
+    for n in ("dq", "dk", "dv"):
+        assert float(np.abs(exp[n]).max()) > 0, f"{n} reference is vacuously zero"
+    e = max_err(got["lse"], exp["lse"])
+    assert e <= LSE_ABS, f"{w.name}{where}: lse max-abs err {e:.3e}"
+
+
+def assert_exact_zeros(w: wl.Workload, inputs: dict, got: dict, q_heads=None):
+    """Fully-masked query rows: O = 0, LSE = 0, dQ = 0 exactly. Hidden key columns: dK = dV = 0 exactly."""
+    mask, kind = inputs["mask"], inputs["mask_kind"]
+    if mask is None:
+        return
+    hidden = (mask == 0) if kind == "bool" else ~(mask > -1e9)
+    dead_rows = hidden.all(axis=2)    # [Bm, Sq]
+    dead_cols = hidden.all(axis=1)    # [Bm, Sk]
+    for b in range(w.B):
+        mb = b if mask.shape[0] > 1 else 0
+        rows = np.nonzero(dead_rows[mb])[0]
+        if rows.size:
+            assert np.all(got["o"][b][:, rows] == 0) and np.all(got["lse"][b][:, rows] == 0)
+            assert np.all(got["dq"][b][:, rows] == 0)
+        cols = np.nonzero(dead_cols[mb])[0]
+        if cols.size and not w.accum:
+            assert np.all(got["dk"][b][:, cols] == 0) and np.all(got["dv"][b][:, cols] == 0)
+        if cols.size and w.accum:
+            np.testing.assert_array_equal(got["dk"][b][:, cols], inputs["dk_acc"][b][:, cols])

@@ -1,0 +1,113 @@
+"""GPU parity: the CUDA path (called through the C-ABI) against the fp64 oracle
+on the same seeded inputs, element by element."""
+import numpy as np
+import pytest
+import torch
+
+from backward_adapter_gb300 import fa_train as ft
+from backward_adapter_gb300 import workloads as wl
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+W = wl.Workload
+SMALL = [
+    wl.TINY_F32,
+    W("f32_causal_offset_d128", B=1, Hq=4, Hkv=2, Sq=70, Sk=150, D=128, dtype="f32", causal=True,
+      q_offset=80, seed=11),
+    W("f32_bool_mask_gqa", B=2, Hq=4, Hkv=1, Sq=45, Sk=97, D=64, dtype="f32", mask="random_bool", seed=12),
+    W("bf16_plain_d64_ragged", B=2, Hq=4, Hkv=2, Sq=200, Sk=333, D=64, seed=13),
+    W("bf16_causal_d128", B=1, Hq=4, Hkv=1, Sq=300, Sk=300, D=128, causal=True, seed=14),
+    W("bf16_causal_offset_accum", B=1, Hq=4, Hkv=2, Sq=130, Sk=517, D=128, causal=True, q_offset=387,
+      accum=True, seed=15),
+    W("bf16_random_add_mask_d64", B=2, Hq=2, Hkv=2, Sq=257, Sk=190, D=64, mask="random_add", seed=16),
+    W("bf16_random_bool_d128", B=2, Hq=4, Hkv=1, Sq=129, Sk=385, D=128, mask="random_bool", seed=17),
+    W("bf16_mask_and_causal", B=1, Hq=2, Hkv=1, Sq=200, Sk=260, D=128, mask="random_add", causal=True,
+      q_offset=60, seed=18),
+    W("bf16_pad_self_small", B=1, Hq=4, Hkv=2, Sq=300, Sk=300, D=64, mask="pad_self", seed=19),
+    W("bf16_cross_small", B=2, Hq=2, Hkv=2, Sq=260, Sk=256, D=128, mask="cross", seed=20),
+    W("bf16_single_key", B=1, Hq=2, Hkv=1, Sq=33, Sk=1, D=64, seed=21),
+    W("bf16_single_query", B=1, Hq=2, Hkv=2, Sq=1, Sk=700, D=128, causal=True, q_offset=699, seed=22),
+    W("bf16_long_keys_small_q", B=1, Hq=4, Hkv=1, Sq=64, Sk=5000, D=128, causal=True, q_offset=4936,
+      accum=True, seed=23),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_workloads_match_oracle(w):
+    inputs = wl.make_inputs(w)
+    got = pu.run_gpu(w, pu.to_device(inputs, w))
+    exp = pu.run_oracle(w, inputs)
+    pu.assert_parity(w, got, exp)
+    pu.assert_exact_zeros(w, inputs, got)
+
+
+def test_broadcast_mask_over_batch():
+    w = W("bf16_bcast_mask", B=2, Hq=2, Hkv=1, Sq=150, Sk=140, D=64, mask="random_add", seed=24)
+    inputs = wl.make_inputs(w)
+    inputs["mask"] = inputs["mask"][:1].copy()
+    got = pu.run_gpu(w, pu.to_device(inputs, w))
+    exp = pu.run_oracle(w, inputs)
+    pu.assert_parity(w, got, exp)
+
+
+def test_empty_query_chunk_zeroes_gradients():
+    w = W("bf16_empty", B=1, Hq=2, Hkv=1, Sq=0, Sk=100, D=64, seed=25)
+    t = pu.to_device(wl.make_inputs(w), w)
+    o, lse = ft.fwd(t["q"], t["k"], t["v"])
+    dk = torch.full_like(t["k"], 7.0)
+    dv = torch.full_like(t["v"], 7.0)
+    ft.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and torch.all(dk == 0) and torch.all(dv == 0)
+
+
+def test_dirty_pad_is_bitwise_invisible():
+    """Garbage in hidden key/value columns leaves every output bit-identical."""
+    w = W("bf16_dirty_pad", B=2, Hq=4, Hkv=2, Sq=256, Sk=256, D=128, mask="cross", seed=26)
+    inputs = wl.make_inputs(w)
+    t = pu.to_device(inputs, w)
+    a = pu.run_gpu(w, t)
+    lens = wl.cross_lengths(w)
+    for b in range(w.B):
+        t["k"][b, :, lens[b]:] = 300.0
+        t["v"][b, :, lens[b]:] = -200.0
+    bb = pu.run_gpu(w, t)
+    for n in ("o", "lse", "dq"):
+        assert np.array_equal(a[n], bb[n]), n
+    for b in range(w.B):
+        assert np.array_equal(a["dk"][b, :, :lens[b]], bb["dk"][b, :, :lens[b]])
+        assert np.array_equal(a["dv"][b, :, :lens[b]], bb["dv"][b, :, :lens[b]])
+
+
+def test_dk_dv_are_deterministic():
+    w = W("bf16_determinism", B=1, Hq=8, Hkv=2, Sq=512, Sk=512, D=128, causal=True, seed=27)
+    t = pu.to_device(wl.make_inputs(w), w)
+    a, b = pu.run_gpu(w, t), pu.run_gpu(w, t)
+    for n in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(a[n], b[n]), n
+
+
+# ---- full-size workloads ------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w", [wl.DIT_SELF, wl.DIT_CROSS], ids=lambda w: w.name)
+def test_full_dit_workloads_match_oracle(w):
+    inputs = wl.make_inputs(w)
+    got = pu.run_gpu(w, pu.to_device(inputs, w))
+    exp = pu.run_oracle(w, inputs)
+    pu.assert_parity(w, got, exp)
+    pu.assert_exact_zeros(w, inputs, got)
+
+
+@pytest.mark.parametrize("w", [wl.CAUSAL_LM, wl.LONG_WINDOW], ids=lambda w: w.name)
+def test_full_size_workloads_match_oracle_on_first_and_last_group(w):
+    """At full size the oracle checks the first and last GQA group (every output they own)."""
+    inputs = wl.make_inputs(w)
+    got = pu.run_gpu(w, pu.to_device(inputs, w))
+    G = w.Hq // w.Hkv
+    for kv in (0, w.Hkv - 1):
+        qh = list(range(kv * G, (kv + 1) * G))
+        exp = pu.run_oracle(w, inputs, q_heads=qh, kv_heads=[kv])
+        sub = {"o": got["o"][:, qh], "lse": got["lse"][:, qh], "dq": got["dq"][:, qh],
+               "dk": got["dk"][:, [kv]], "dv": got["dv"][:, [kv]]}
+        pu.assert_parity(w, sub, exp, where=f" kv-head {kv}")
