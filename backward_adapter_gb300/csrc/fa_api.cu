@@ -113,7 +113,13 @@ fa_status cuda_status(cudaError_t e, const char* what) {
 }
 
 // The tcgen05 path takes bf16 inputs; fp32 inputs stay on the SIMT fp32 path.
-bool use_tensor_cores(const Shape& s) { return s.dtype == DT_BF16 && tc_supported(s); }
+bool use_tc_fwd(const Shape& s) { return s.dtype == DT_BF16 && tc_fwd_supported(s); }
+bool use_tc_bwd(const Shape& s) { return s.dtype == DT_BF16 && tc_bwd_supported(s); }
+
+// Status word of the bounded device waits (0 = fine; 0x80000000 | site = a wait ran out).
+__device__ unsigned int g_fa_device_status = 0;
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
 
 thread_local cudaEvent_t g_prof_start[KID_COUNT] = {};
 thread_local cudaEvent_t g_prof_stop[KID_COUNT] = {};
@@ -129,9 +135,20 @@ cudaError_t prof_end(int kid, cudaStream_t st) {
 }
 void count_launches(int n) { g_launches += (uint64_t)n; }
 
+unsigned* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
 FwdPlan plan_fwd(const Shape& s) {
   FwdPlan p{};
-  p.tensor_core = use_tensor_cores(s);
+  p.tensor_core = use_tc_fwd(s);
   p.kv_splits = p.tensor_core ? tc_fwd_kv_splits(s) : 1;
   size_t off = 0;
   if (p.tensor_core && s.mask_kind != MK_NONE) {
@@ -154,7 +171,7 @@ FwdPlan plan_fwd(const Shape& s) {
 
 BwdPlan plan_bwd(const Shape& s) {
   BwdPlan p{};
-  p.tensor_core = use_tensor_cores(s);
+  p.tensor_core = use_tc_bwd(s);
   size_t off = 0;
   const size_t rows = (size_t)s.B * s.Hq * s.Sq;
   if (p.tensor_core && s.mask_kind != MK_NONE) {
@@ -280,5 +297,16 @@ fa_status fa_profile_set_events(int kernel, void* start_event, void* stop_event)
 }
 
 uint64_t fa_profile_launch_count(void) { return g_launches; }
+
+fa_status fa_device_status(uint32_t* out) {
+  if (out == nullptr) { set_error("out is NULL"); return FA_ERR_INVALID_ARG; }
+  unsigned* p = device_status_ptr();
+  if (p == nullptr) { set_error("no CUDA device"); return FA_ERR_CUDA; }
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v != 0) e = cudaMemset(p, 0, sizeof(v));
+  *out = v;
+  return cuda_status(e, "read device status");
+}
 
 }  // extern "C"

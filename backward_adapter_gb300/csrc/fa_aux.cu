@@ -82,11 +82,13 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   store8(dq + i * 8, x);
 }
 
-// One block per (mask batch, q-tile, k-tile) of 128 x 128.
+// One block per (mask batch, q-tile, k-tile) of 128 x 128, flattened in that order.
 __global__ void __launch_bounds__(256) mask_classify_kernel(Shape s, const void* __restrict__ mask,
-                                                            uint8_t* __restrict__ tilemap) {
-  const int kt = blockIdx.x, qt = blockIdx.y, mb = blockIdx.z;
-  const int nqt = gridDim.y, nkt = gridDim.x;
+                                                            uint8_t* __restrict__ tilemap, int nqt, int nkt) {
+  const long long tile = blockIdx.x;
+  const int kt = (int)(tile % nkt);
+  const int qt = (int)((tile / nkt) % nqt);
+  const int mb = (int)(tile / ((long long)nkt * nqt));
   bool any_vis = false, all_open = true;
   for (int e = threadIdx.x; e < 128 * 128; e += 256) {
     const int i = qt * 128 + e / 128, j = kt * 128 + e % 128;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(256) mask_classify_kernel(Shape s, const void*
   any_vis = __syncthreads_or(any_vis);
   all_open = __syncthreads_and(all_open);
   if (threadIdx.x == 0)
-    tilemap[((size_t)mb * nqt + qt) * nkt + kt] = !any_vis ? TILE_SKIP : (all_open ? TILE_OPEN : TILE_MIXED);
+    tilemap[tile] = !any_vis ? TILE_SKIP : (all_open ? TILE_OPEN : TILE_MIXED);
 }
 
 }  // namespace
@@ -157,10 +159,12 @@ cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc) {
 
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st) {
   if (s.mask_kind == MK_NONE || s.Sq == 0) return cudaSuccess;
-  dim3 grid((s.Sk + 127) / 128, (s.Sq + 127) / 128, s.mask_batch);
+  const int nqt = (s.Sq + 127) / 128, nkt = (s.Sk + 127) / 128;
+  const long long tiles = (long long)s.mask_batch * nqt * nkt;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = prof_begin(KID_MASK, st);
   if (e != cudaSuccess) return e;
-  mask_classify_kernel<<<grid, 256, 0, st>>>(s, mask, tilemap);
+  mask_classify_kernel<<<(unsigned)tiles, 256, 0, st>>>(s, mask, tilemap, nqt, nkt);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_MASK, st);

@@ -68,6 +68,9 @@ struct BwdPlan {
   size_t total;
 };
 
+// Device status word the kernels' bounded waits report into (nullptr if unavailable).
+unsigned* device_status_ptr();
+
 // Tracing hooks (fa_profile_set_events): per-thread events recorded around a
 // kernel family, and a per-thread launch counter.
 enum : int { KID_FWD = 0, KID_BWD_MAIN = 1, KID_BWD_DSUM = 2, KID_BWD_DQCONV = 3, KID_MASK = 4, KID_COUNT = 5 };
@@ -88,7 +91,9 @@ cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc);
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
 
 // tcgen05 paths (bf16, D in {64, 128}).
-bool tc_supported(const Shape& s);
+bool tc_fwd_supported(const Shape& s);
+bool tc_bwd_supported(const Shape& s);
+cudaError_t make_tmap_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D);
 int tc_fwd_kv_splits(const Shape& s);
 cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);
 cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws);

@@ -1,0 +1,572 @@
+// Forward of the fused attention training op on the 5th-generation tensor
+// cores (tcgen05, sm_103a): O = softmax(scale * Q K^T + mask) V and the per-row
+// LSE (flash-attn-training skill, trap list item 9: a fully-masked row gives
+// O = 0 and LSE = 0; llama.cpp PR #57, commit 86c140d: the backward needs LSE).
+//
+// One CTA takes 256 query rows (two 128-row tiles Q0, Q1) of one (batch, query
+// head) and walks the visible 128-key tiles of its key/value head:
+//   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of slots;
+//   warp 1      MMA issuer (one thread) and TMEM owner:
+//                 S_t = Q_t K_j^T  (SMEM x SMEM -> TMEM fp32)
+//                 O_t += P_t V_j   (P from TMEM, V from SMEM -> TMEM fp32);
+//   warps 4-7   softmax for Q0, warps 8-11 softmax for Q1: a thread owns one
+//               query row, reads its 128 scores from TMEM, applies scale, mask
+//               and the causal rule, keeps the running max / sum in the log2
+//               domain and writes P (bf16) back into TMEM over its scores.
+// The two softmax groups ping-pong: while one works on its scores, the tensor
+// core runs the other tile's S and PV MMAs. O is rescaled in TMEM only when a
+// row's running max grows by more than 2^8 (otherwise P keeps the older max,
+// which bounds P by 256 and leaves O, l and LSE consistent).
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
+// Long key windows with few query rows split the keys over CTAs; each split
+// writes unnormalised (O, m, l) partials and a combine kernel merges them.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+#include "tc_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;        // query rows per tile
+constexpr int kBN = 128;        // keys per tile
+constexpr int kRowsPerCta = 2 * kBM;
+constexpr int kThreads = 384;   // 12 warps
+constexpr int kNumSms = 152;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+struct FwdTcParams {
+  CUtensorMap tm_q, tm_k, tm_v;
+  Shape s;
+  const void* mask;
+  const uint8_t* tilemap;   // [mask_batch, nqt, nkt] or null
+  __nv_bfloat16* o;
+  float* lse;
+  float* part_o;            // [splits, rows, D] when split
+  float* part_ml;           // [splits, rows, 2] when split
+  int kv_splits;
+  int n_qpairs;
+  int nqt, nkt;
+  unsigned* status;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16 (one 128B-swizzled box)
+  static constexpr int kTileBytes = kBM * D * 2;         // one Q or K or V tile
+  static constexpr int kSlots = D == 128 ? 4 : 8;        // ring slots for K and V tiles
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+  static constexpr int kBytes = kBarOff + 256 + 1024;    // barriers + alignment slack
+};
+
+// Key-tile range of a CTA after causal clipping and the split.
+struct KvRange {
+  int begin, end;  // tile indices [begin, end)
+};
+
+__device__ __forceinline__ KvRange kv_range(const FwdTcParams& p, int q_row0, int split) {
+  const Shape& s = p.s;
+  long long kv_end = s.Sk;
+  if (s.causal) {
+    const long long last_row = (long long)min(q_row0 + kRowsPerCta, s.Sq) - 1;
+    kv_end = min(kv_end, s.q_offset + last_row + 1);
+  }
+  const int n = (int)((kv_end + kBN - 1) / kBN);
+  const int per = (n + p.kv_splits - 1) / p.kv_splits;
+  KvRange r;
+  r.begin = min(n, split * per);
+  r.end = min(n, r.begin + per);
+  return r;
+}
+
+// Tile-map code of (query tile qt, key tile j), TILE_OPEN without a mask.
+__device__ __forceinline__ int tile_code(const FwdTcParams& p, int mb, int qt, int j) {
+  if (p.tilemap == nullptr) return TILE_OPEN;
+  if (qt >= p.nqt) return TILE_SKIP;
+  return p.tilemap[((size_t)mb * p.nqt + qt) * p.nkt + j];
+}
+
+__device__ __forceinline__ bool skip_tile(const FwdTcParams& p, int mb, int qt0, int j) {
+  return tile_code(p, mb, qt0, j) == TILE_SKIP && tile_code(p, mb, qt0 + 1, j) == TILE_SKIP;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdTcParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + L::kQOff;
+  uint8_t* sKV = smem + L::kKVOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* bar_q = bars + 0;
+  uint64_t* bar_full = bars + 1;                  // [kSlots]
+  uint64_t* bar_empty = bar_full + L::kSlots;     // [kSlots]
+  uint64_t* bar_s = bar_empty + L::kSlots;        // [2]
+  uint64_t* bar_p = bar_s + 2;                    // [2]
+  uint64_t* bar_o = bar_p + 2;                    // [2]
+  uint64_t* bar_done = bar_o + 2;                 // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Shape& s = p.s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work unit: heaviest query-row pairs first (causal work grows with the row index)
+  const int BH = s.B * s.Hq;
+  const int split = blockIdx.x % p.kv_splits;
+  const int rest = blockIdx.x / p.kv_splits;
+  const int bh = rest % BH;
+  const int qpair = p.n_qpairs - 1 - rest / BH;
+  const int b = bh / s.Hq, h = bh % s.Hq;
+  const int kvh = h / (s.Hq / s.Hkv);
+  const int q_row0 = qpair * kRowsPerCta;
+  const int qt0 = q_row0 / kBM;
+  const int mb = s.mask_batch > 1 ? b : 0;
+  const KvRange kr = kv_range(p, q_row0, split);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < L::kSlots; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 4);
+      mbar_init(&bar_o[t], 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      mbar_arrive_expect_tx(bar_q, 2 * L::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int box = 0; box < D / 64; ++box)
+          tma_load_3d(sQ + t * L::kTileBytes + box * L::kBoxBytes, &p.tm_q, bar_q, box * 64, q_row0 + t * kBM, bh);
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t used_mask = 0, phase_mask = 0;  // per slot: filled at least once / parity of its last fill
+      const int kvrow = b * s.Hkv + kvh;
+      for (int j = kr.begin; j < kr.end; ++j) {
+        if (skip_tile(p, mb, qt0, j)) continue;
+        bool ok = true;
+        for (int which = 0; which < 2 && ok; ++which) {
+          if (!mbar_wait(&bar_empty[slot], phase ^ 1, abort_flag, p.status, 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar_full[slot], L::kTileBytes);
+          const CUtensorMap* map = which == 0 ? &p.tm_k : &p.tm_v;
+          for (int box = 0; box < D / 64; ++box)
+            tma_load_3d(sKV + slot * L::kTileBytes + box * L::kBoxBytes, map, &bar_full[slot], box * 64, j * kBN,
+                        kvrow);
+          used_mask |= 1u << slot;
+          phase_mask = (phase_mask & ~(1u << slot)) | (phase << slot);
+          if (++slot == L::kSlots) { slot = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // Drain: every copy this thread issued has landed before the block can exit.
+      mbar_wait(bar_q, 0, nullptr, p.status, 2);
+      for (int i = 0; i < L::kSlots; ++i)
+        if (used_mask >> i & 1u) mbar_wait(&bar_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 3);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
+      const uint32_t tS[2] = {tmem + 0, tmem + 128};
+      const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      bool ok = mbar_wait(bar_q, 0, abort_flag, p.status, 10);
+      tc_fence_after();
+      int idx = 0, c = 0;  // tiles processed, slots consumed
+      int v_slot = 0;
+      uint32_t v_phase = 0;
+      for (int j = kr.begin; ok && j < kr.end; ++j) {
+        if (skip_tile(p, mb, qt0, j)) continue;
+        const int k_slot = c % L::kSlots;
+        const uint32_t k_phase = (c / L::kSlots) & 1;
+        if (!(ok = mbar_wait(&bar_full[k_slot], k_phase, abort_flag, p.status, 11))) break;
+        tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (idx > 0) {
+            if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 12))) break;
+            if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 13))) break;
+            tc_fence_after();
+            const uint32_t vbase = sKVa + v_slot * L::kTileBytes;
+#pragma unroll
+            for (int k = 0; k < kBN / 16; ++k)
+              mma_ts(tO[t], tS[t] + k * 8, smem_desc_sw128(vbase + k * 16 * 128, L::kBoxBytes, 1024), idesc_pv,
+                     (idx - 1 > 0 || k > 0) ? 1u : 0u);
+          }
+          const uint32_t qbase = sQa + t * L::kTileBytes;
+          const uint32_t kbase = sKVa + k_slot * L::kTileBytes;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * L::kBoxBytes + (k % 4) * 32;
+            mma_ss(tS[t], smem_desc_sw128(qbase + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024), idesc_qk,
+                   k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_s[t]);
+        }
+        if (!ok) break;
+        if (idx > 0) mma_commit(&bar_empty[v_slot]);
+        mma_commit(&bar_empty[k_slot]);
+        v_slot = (c + 1) % L::kSlots;
+        v_phase = ((c + 1) / L::kSlots) & 1;
+        c += 2;
+        ++idx;
+      }
+      if (ok && idx > 0) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 14))) break;
+          if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 15))) break;
+          tc_fence_after();
+          const uint32_t vbase = sKVa + v_slot * L::kTileBytes;
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            mma_ts(tO[t], tS[t] + k * 8, smem_desc_sw128(vbase + k * 16 * 128, L::kBoxBytes, 1024), idesc_pv,
+                   (idx - 1 > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar_o[t]);
+        }
+      }
+      // Every MMA this thread issued is complete before TMEM is released.
+      mma_commit(bar_done);
+      mbar_wait(bar_done, 0, nullptr, p.status, 16);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax, one row per thread
+    const int t = (warp - 4) / 4;
+    const int wq = warp & 3;                       // TMEM lane slice of this warp
+    const int r = wq * 32 + lane;                  // row within the query tile
+    const int i = q_row0 + t * kBM + r;            // query row
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + t * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + t * D + lane_off;
+    const float sl2 = s.scale * kLog2e;
+    const long long causal_lim = s.causal ? s.q_offset + i : (long long)INT32_MAX;
+    const size_t mrow = ((size_t)mb * s.Sq + (size_t)min(i, s.Sq - 1)) * (size_t)s.Sk;
+    float m = -CUDART_INF_F, l = 0.f;
+    int idx = 0;
+    bool ok = true;
+    for (int j = kr.begin; j < kr.end; ++j) {
+      if (skip_tile(p, mb, qt0, j)) continue;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], idx & 1, abort_flag, p.status, 20)))) break;
+      tc_fence_after();
+      // scale into the log2 domain, then hide what the mask, the causal rule or the key tail hides
+      const int code = tile_code(p, mb, qt0 + t, j);
+      const int key0 = j * kBN;
+      const bool dead = (code == TILE_SKIP) || i >= s.Sq;
+      const bool full = !dead && code == TILE_OPEN && key0 + kBN <= s.Sk && key0 + kBN - 1 <= causal_lim;
+      // x_e = log2(e) * (scale * s_e + bias_e), or -inf where the pair is hidden
+      auto masked = [&](uint32_t (&raw)[32], int c0, float (&x)[32]) {
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(raw[e]) * sl2;
+        } else if (dead) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = -CUDART_INF_F;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int key = key0 + c0 + e;
+            bool vis = key < s.Sk && key <= causal_lim;
+            float bias = 0.f;
+            if (vis && code == TILE_MIXED) {
+              if (s.mask_kind == MK_ADD) {
+                const float mv = static_cast<const float*>(p.mask)[mrow + key];
+                vis = mv > kMaskFloor;
+                bias = mv * kLog2e;
+              } else {
+                vis = static_cast<const uint8_t*>(p.mask)[mrow + key] != 0;
+              }
+            }
+            x[e] = vis ? fmaf(__uint_as_float(raw[e]), sl2, bias) : -CUDART_INF_F;
+          }
+        }
+      };
+      // pass 1: row max of this tile
+      // (TMEM loads and stores are warp-collective: every lane issues them, hidden rows just get -inf)
+      float tmax = -CUDART_INF_F;
+#pragma unroll
+      for (int cch = 0; cch < kBN / 32; ++cch) {
+        uint32_t raw[32];
+        float x[32];
+        tmem_ld32(tS + cch * 32, raw);
+        tmem_wait_ld();
+        reg_fence(raw);
+        masked(raw, cch * 32, x);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, x[e]);
+      }
+      const float m_new = fmaxf(m, tmax);
+      const bool rescale = m_new > m + kRescaleThreshold;   // false while nothing is visible
+      const float m_use = rescale ? m_new : m;
+      const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;
+      const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+      // pass 2: P = 2^(x - m) as bf16 over the first 64 columns of the score block; chunk c of
+      // the scores is read before P chunk c lands on columns [16c, 16c + 16) (already read)
+      float sum = 0.f;
+#pragma unroll
+      for (int cch = 0; cch < kBN / 32; ++cch) {
+        uint32_t pk[16];
+        uint32_t raw[32];
+        float x[32];
+        tmem_ld32(tS + cch * 32, raw);
+        tmem_wait_ld();
+        reg_fence(raw);
+        masked(raw, cch * 32, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(x[2 * e] - m_sub);
+          const float p1 = ex2_approx(x[2 * e + 1] - m_sub);
+          sum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + cch * 16, pk);
+      }
+      l = l * alpha + sum;
+      m = m_use;
+      if (__any_sync(0xffffffffu, rescale) && idx > 0) {  // alpha = 1 on rows that keep their max
+        // O already holds P V of the earlier tiles (their MMAs finished before these scores did).
+#pragma unroll
+        for (int cch = 0; cch < D / 32; ++cch) {
+          uint32_t ov[32];
+          tmem_ld32(tO + cch * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tO + cch * 32, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[t]);
+      ++idx;
+    }
+    // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2; a row with nothing visible gets 0 and 0
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && idx > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], 0, abort_flag, p.status, 21));
+    tc_fence_after();
+    if (ok) {
+      const bool row_ok = i < s.Sq;
+      const size_t row = (size_t)bh * s.Sq + (row_ok ? i : 0);
+      const bool alive = l > 0.f;
+      if (p.kv_splits == 1) {
+        const float inv = alive ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + row * D);
+#pragma unroll
+        for (int cch = 0; cch < D / 32; ++cch) {
+          uint32_t ov[32];
+          if (idx > 0) {
+            tmem_ld32(tO + cch * 32, ov);
+            tmem_wait_ld();
+            reg_fence(ov);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          }
+          uint32_t pkd[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pkd[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+          if (row_ok) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[cch * 4 + v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          }
+        }
+        if (row_ok) p.lse[row] = alive ? (m + __log2f(l)) * kLn2 : 0.f;
+      } else {
+        const size_t rows = (size_t)s.B * s.Hq * s.Sq;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)split * rows + row) * D);
+#pragma unroll
+        for (int cch = 0; cch < D / 32; ++cch) {
+          uint32_t ov[32];
+          if (idx > 0) {
+            tmem_ld32(tO + cch * 32, ov);
+            tmem_wait_ld();
+            reg_fence(ov);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[cch * 8 + v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                              __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+          }
+        }
+        if (row_ok) {
+          float2* ml = reinterpret_cast<float2*>(p.part_ml + ((size_t)split * rows + row) * 2);
+          *ml = make_float2(alive ? m : -CUDART_INF_F, l);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge split-KV partials: m = max m_s, l = sum l_s 2^(m_s - m), O = sum O_s 2^(m_s - m) / l.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ part_o,
+                                                          const float* __restrict__ part_ml, int splits,
+                                                          long long rows, __nv_bfloat16* __restrict__ o,
+                                                          float* __restrict__ lse) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int E = D / 32;
+  float mmax = -CUDART_INF_F;
+  for (int sp = 0; sp < splits; ++sp) mmax = fmaxf(mmax, part_ml[((size_t)sp * rows + row) * 2]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  if (mmax != -CUDART_INF_F) {
+    for (int sp = 0; sp < splits; ++sp) {
+      const float ms = part_ml[((size_t)sp * rows + row) * 2];
+      if (ms == -CUDART_INF_F) continue;
+      const float w = ex2_approx(ms - mmax);
+      l += part_ml[((size_t)sp * rows + row) * 2 + 1] * w;
+      const float* src = part_o + ((size_t)sp * rows + row) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += src[e] * w;
+    }
+  }
+  const bool alive = l > 0.f;
+  const float inv = alive ? 1.f / l : 0.f;
+  __nv_bfloat16* dst = o + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+  if (lane == 0) lse[row] = alive ? (mmax + __log2f(l)) * kLn2 : 0.f;
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int n_qpairs(const Shape& s) { return (s.Sq + kRowsPerCta - 1) / kRowsPerCta; }
+
+int kv_tiles_total(const Shape& s) {
+  long long kv_end = s.Sk;
+  if (s.causal) kv_end = min(kv_end, s.q_offset + s.Sq);
+  return (int)((kv_end + kBN - 1) / kBN);
+}
+
+}  // namespace
+
+// bf16 [rows-of-D] tensor viewed as (D, S, heads), boxes of 64 x 128 x 1 with 128-byte swizzle.
+cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D) {
+  static EncodeTiledFn encode = nullptr;
+  if (encode == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+bool tc_fwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq > 0; }
+
+int tc_fwd_kv_splits(const Shape& s) {
+  const long long units = (long long)s.B * s.Hq * n_qpairs(s);
+  if (units >= kNumSms) return 1;
+  const int by_waves = (int)((4LL * kNumSms) / units);
+  const int by_len = kv_tiles_total(s) / 8;
+  return max(1, min(by_waves, by_len));
+}
+
+template <int D>
+static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, unsigned* status) {
+  const Shape& s = a.s;
+  FwdTcParams p;
+  cudaError_t e;
+  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D)) != cudaSuccess) return e;
+  p.s = s;
+  p.mask = a.mask;
+  p.nqt = (s.Sq + kBM - 1) / kBM;
+  p.nkt = (s.Sk + kBN - 1) / kBN;
+  p.tilemap = nullptr;
+  if (s.mask_kind != MK_NONE) {
+    uint8_t* tm = reinterpret_cast<uint8_t*>(ws + plan.tilemap_off);
+    if ((e = launch_mask_classify(s, a.mask, tm, a.stream)) != cudaSuccess) return e;
+    p.tilemap = tm;
+  }
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.kv_splits = plan.kv_splits;
+  p.part_o = plan.kv_splits > 1 ? reinterpret_cast<float*>(ws + plan.part_o_off) : nullptr;
+  p.part_ml = plan.kv_splits > 1 ? reinterpret_cast<float*>(ws + plan.part_ml_off) : nullptr;
+  p.n_qpairs = n_qpairs(s);
+  p.status = status;
+  const int smem = FwdSmem<D>::kBytes;
+  if ((e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  const long long ctas = (long long)s.B * s.Hq * p.n_qpairs * plan.kv_splits;
+  if ((e = prof_begin(KID_FWD, a.stream)) != cudaSuccess) return e;
+  fwd_tc_kernel<D><<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (plan.kv_splits > 1) {
+    const long long rows = (long long)s.B * s.Hq * s.Sq;
+    fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(p.part_o, p.part_ml, plan.kv_splits,
+                                                                            rows, p.o, p.lse);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return prof_end(KID_FWD, a.stream);
+}
+
+cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws) {
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorUnknown;
+  return a.s.D == 64 ? tc_fwd_t<64>(a, plan, ws, status) : tc_fwd_t<128>(a, plan, ws, status);
+}
+
+}  // namespace fa

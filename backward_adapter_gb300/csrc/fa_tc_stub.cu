@@ -1,7 +1,5 @@
 #include "fa_internal.h"
 namespace fa {
-bool tc_supported(const Shape&) { return false; }
-int tc_fwd_kv_splits(const Shape&) { return 1; }
-cudaError_t tc_fwd(const FwdArgs&, const FwdPlan&, char*) { return cudaErrorNotSupported; }
+bool tc_bwd_supported(const Shape&) { return false; }
 cudaError_t tc_bwd(const BwdArgs&, const BwdPlan&, char*) { return cudaErrorNotSupported; }
 }

@@ -23,7 +23,7 @@ FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
-            "fa_profile_launch_count")
+            "fa_profile_launch_count", "fa_device_status")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_profile_set_events.restype = st
     lib.fa_profile_launch_count.argtypes = []
     lib.fa_profile_launch_count.restype = ctypes.c_uint64
+    lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.fa_device_status.restype = st
     _lib = lib
     return lib
 
@@ -220,3 +222,10 @@ def profile_set_events(kernel: int, start=None, stop=None) -> None:
 def profile_launch_count() -> int:
     """Kernels the library has launched from this thread so far."""
     return int(load_library().fa_profile_launch_count())
+
+
+def device_status() -> int:
+    """Read and clear the kernels' status word (0 = every bounded wait completed)."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().fa_device_status(ctypes.byref(v)))
+    return int(v.value)

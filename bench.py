@@ -231,6 +231,10 @@ def run_reference(args):
 # the GPU path
 # ---------------------------------------------------------------------------------------------
 
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9 if ms > 0 else None
+
+
 def run_ours(args):
     import torch
 
@@ -304,7 +308,14 @@ def run_ours(args):
     clock_info = clocks.stop()
 
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    kern_ms = {kid: statistics.mean(a.elapsed_time(b) for a, b in evs) for kid, evs in kern.items()}
+
+    def mean_or_zero(evs):
+        try:
+            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+        except (RuntimeError, ValueError):  # this path does not launch that kernel
+            return 0.0
+
+    kern_ms = {kid: mean_or_zero(evs) for kid, evs in kern.items()}
     mean_ms = max_over_ranks(world, statistics.mean(step_ms))
     value = world * fl["total"] / (mean_ms * 1e-3) / 1e12
 
@@ -374,8 +385,8 @@ def run_ours(args):
                                     kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]) * 1e-3) / 1e12,
         "kernel_ms": {"fwd": fwd_ms, "bwd_main": bwd_main_ms, "bwd_dsum": kern_ms[ft.FA_KERNEL_BWD_DSUM],
                       "bwd_dq_convert": kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]},
-        "hbm_passes_gbs": {"bwd_dsum": dsum_bytes / (kern_ms[ft.FA_KERNEL_BWD_DSUM] * 1e-3) / 1e9,
-                           "bwd_dq_convert": dqconv_bytes / (kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT] * 1e-3) / 1e9,
+        "hbm_passes_gbs": {"bwd_dsum": gbs(dsum_bytes, kern_ms[ft.FA_KERNEL_BWD_DSUM]),
+                           "bwd_dq_convert": gbs(dqconv_bytes, kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]),
                            "peak": peaks["hbm_gbs"]},
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,

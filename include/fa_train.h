@@ -156,6 +156,15 @@ FA_API fa_status fa_profile_set_events(int kernel, void* start_event, void* stop
 /* Number of CUDA kernels the library has launched from the calling thread so far. */
 FA_API uint64_t fa_profile_launch_count(void);
 
+/*
+ * Reads and clears the status word of the current device's kernels: 0 when
+ * every wait inside a kernel completed; otherwise 0x80000000 | site, where site
+ * names the wait that ran out of its time limit (the kernel then stopped early
+ * and its outputs are invalid). Synchronous (waits for the device to finish the
+ * copy). Returns FA_ERR_CUDA if no device is usable.
+ */
+FA_API fa_status fa_device_status(uint32_t* out);
+
 /* Static description of a status code. */
 FA_API const char* fa_status_str(fa_status s);
 
