@@ -1,0 +1,569 @@
+// Backward of the fused attention training op on the 5th-generation tensor
+// cores (tcgen05, sm_103a). With P recomputed from LSE, D_i = <dO_i, O_i>
+// precomputed, and dS = P (dP - D) (llama.cpp PR #57, commit 86c140d:
+// "LSE, D, then grads per tile; GQA group-sum"):
+//     dV_j = sum_{h in group} sum_i P_ij dO_i
+//     dK_j = scale sum_{h in group} sum_i dS_ij q_i
+//     dQ_i = scale sum_j dS_ij k_j
+//
+// One CTA owns a 128-key tile of one (batch, key/value head). Its dK and dV
+// live in TMEM for the whole walk (no atomics on them: the ownership split is by
+// key tile), while it walks every query tile of every query head of the GQA
+// group that can see its keys. Per step (BQ query rows):
+//     S^T  = K Q^T           (SMEM x SMEM -> TMEM)       keys are TMEM lanes
+//     dP^T = V dO^T          (SMEM x SMEM -> TMEM)
+//     softmax-grad warps: P^T = 2^(S^T scale log2e + bias - LSE log2e), 0 where hidden;
+//                         dS^T = P^T (dP^T - D); P^T, dS^T -> TMEM (bf16), dS^T -> SMEM
+//     dV  += P^T dO          (TMEM x SMEM)
+//     dK  += dS^T Q          (TMEM x SMEM)
+//     dQ^T = K^T dS^T  (D = 128)  or  dQ = dS K  (D = 64)   (SMEM x SMEM -> TMEM)
+//     dQ writer warps add the dQ partial into the fp32 dQ accumulator (red.add).
+// Roles: warp 0 TMA (K, V once; Q, dO per step), warp 1 MMA issue + TMEM owner,
+// warp 2 LSE/D staging, warps 4-7 softmax-grad (a thread owns one key),
+// warps 8-11 dQ writer. With D = 128 the S/dP TMEM block is double-buffered so
+// the next step's S^T, dP^T run on the tensor core while the softmax-grad warps
+// work on the current one.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+#include "tc_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace tc;
+
+constexpr int kBN = 128;       // keys per CTA
+constexpr int kThreads = 384;  // 12 warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BQ = D == 128 ? 64 : 128;        // query rows per step
+  static constexpr int NBUF = D == 128 ? 2 : 1;         // S/dP TMEM blocks
+  static constexpr int BUF_COLS = 2 * BQ;               // S^T [0,BQ), dP^T [BQ,2BQ)
+  static constexpr int P_COL = 0;                       // P^T (bf16) over the first BQ/2 columns
+  static constexpr int DS_COL = D == 128 ? 32 : 128;    // dS^T (bf16)
+  static constexpr int DQ_COL = D == 128 ? 64 : 64;     // dQ^T (D=128: 64 cols) / dQ (D=64: 64 cols)
+  static constexpr int DV_COL = 256;
+  static constexpr int DK_COL = 256 + D;
+  static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
+  static constexpr int NSTAGE = 3;                      // Q/dO ring depth
+  // shared memory (bytes)
+  static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
+  static constexpr int KV_TILE = kBN * D * 2;
+  static constexpr int QBOX = BQ * 128;                 // BQ rows x 128 B
+  static constexpr int Q_TILE = BQ * D * 2;
+  static constexpr int DS_BLOCK = 128 * 128;            // 128 keys x 64 queries (bf16)
+  static constexpr int DS_TILE = (BQ / 64) * DS_BLOCK;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_TILE;
+  static constexpr int OFF_STAGE = 2 * KV_TILE;         // [NSTAGE] x (Q, dO)
+  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // [2] x dS^T
+  static constexpr int OFF_LSED = OFF_DS + 2 * DS_TILE;            // [NSTAGE] x (lse2[BQ], dsum[BQ])
+  static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
+  static constexpr int BYTES = OFF_BAR + 512 + 1024;
+};
+
+struct BwdTcParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  Shape s;
+  const void* mask;
+  const uint8_t* tilemap;
+  const float* lse;
+  const float* dsum;
+  float* dq_acc;
+  void* dk;  // bf16 [B,Hkv,Sk,D], or fp32 accumulator
+  void* dv;
+  int accum;
+  int nqt, nkt;
+  unsigned* status;
+};
+
+// The steps of a CTA: (query head of the group, query tile) pairs in a fixed order.
+struct StepIter {
+  int G, Sq, BQ, ibeg;
+  int hh, i0;
+  __device__ void init(int G_, int Sq_, int BQ_, int ibeg_) {
+    G = G_; Sq = Sq_; BQ = BQ_; ibeg = ibeg_;
+    hh = 0; i0 = ibeg;
+  }
+  __device__ bool valid() const { return hh < G && ibeg < Sq; }
+  __device__ void next() {
+    i0 += BQ;
+    if (i0 >= Sq) { i0 = ibeg; ++hh; }
+  }
+};
+
+__device__ __forceinline__ int bwd_tile_code(const BwdTcParams& p, int mb, int i0, int kt) {
+  if (p.tilemap == nullptr) return TILE_OPEN;
+  return p.tilemap[((size_t)mb * p.nqt + i0 / 128) * p.nkt + kt];
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* bar_kv = bars;                              // 1
+  uint64_t* bar_qdo_full = bar_kv + 1;                  // NSTAGE
+  uint64_t* bar_qdo_empty = bar_qdo_full + C::NSTAGE;   // NSTAGE
+  uint64_t* bar_lsed_full = bar_qdo_empty + C::NSTAGE;  // NSTAGE
+  uint64_t* bar_lsed_empty = bar_lsed_full + C::NSTAGE; // NSTAGE
+  uint64_t* bar_sdp_full = bar_lsed_empty + C::NSTAGE;  // NBUF
+  uint64_t* bar_p_full = bar_sdp_full + C::NBUF;        // NBUF
+  uint64_t* bar_dq_full = bar_p_full + C::NBUF;         // NBUF
+  uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
+  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 2
+  uint64_t* bar_mma_done = bar_ds_free + 2;             // 1
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* lsed = reinterpret_cast<float*>(smem + C::OFF_LSED);
+
+  const Shape& s = p.s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = s.Hq / s.Hkv;
+
+  // ---- work unit: key tile kt of (b, kvh); under the causal rule the low key tiles carry the most work
+  const int kt = blockIdx.x % p.nkt;
+  const int bkv = blockIdx.x / p.nkt;
+  const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
+  const int j0 = kt * kBN;
+  const int mb = s.mask_batch > 1 ? b : 0;
+  int ibeg = 0;
+  if (s.causal) {
+    const long long first = (long long)j0 - s.q_offset;  // rows below this see none of the keys
+    ibeg = first <= 0 ? 0 : (int)((first / BQ) * BQ);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(&bar_qdo_full[i], 1);
+      mbar_init(&bar_qdo_empty[i], 1);
+      mbar_init(&bar_lsed_full[i], 1);
+      mbar_init(&bar_lsed_empty[i], 4);
+    }
+    for (int i = 0; i < C::NBUF; ++i) {
+      mbar_init(&bar_sdp_full[i], 1);
+      mbar_init(&bar_p_full[i], 4);
+      mbar_init(&bar_dq_full[i], 1);
+      mbar_init(&bar_dq_free[i], 4);
+    }
+    mbar_init(&bar_ds_free[0], 1);
+    mbar_init(&bar_ds_free[1], 1);
+    mbar_init(bar_mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto step_skipped = [&](const StepIter& it) { return bwd_tile_code(p, mb, it.i0, kt) == TILE_SKIP; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      prefetch_tmap(&p.tm_do);
+      const int kvrow = b * s.Hkv + kvh;
+      mbar_arrive_expect_tx(bar_kv, 2 * C::KV_TILE);
+      for (int box = 0; box < D / 64; ++box) {
+        tma_load_3d(smem + C::OFF_K + box * C::KV_BOX, &p.tm_k, bar_kv, box * 64, j0, kvrow);
+        tma_load_3d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvrow);
+      }
+      uint32_t used_mask = 0, phase_mask = 0;
+      StepIter it;
+      it.init(G, s.Sq, BQ, ibeg);
+      for (int st = 0; it.valid(); it.next()) {
+        if (step_skipped(it)) continue;
+        const int slot = st % C::NSTAGE;
+        const uint32_t ph = (st / C::NSTAGE) & 1;
+        if (!mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101)) break;
+        mbar_arrive_expect_tx(&bar_qdo_full[slot], 2 * C::Q_TILE);
+        uint8_t* sq = smem + C::OFF_STAGE + slot * 2 * C::Q_TILE;
+        const int qrow = b * s.Hq + kvh * G + it.hh;
+        for (int box = 0; box < D / 64; ++box) {
+          tma_load_3d(sq + box * C::QBOX, &p.tm_q, &bar_qdo_full[slot], box * 64, it.i0, qrow);
+          tma_load_3d(sq + C::Q_TILE + box * C::QBOX, &p.tm_do, &bar_qdo_full[slot], box * 64, it.i0, qrow);
+        }
+        used_mask |= 1u << slot;
+        phase_mask = (phase_mask & ~(1u << slot)) | (ph << slot);
+        ++st;
+      }
+      // drain every copy this thread issued
+      mbar_wait(bar_kv, 0, nullptr, p.status, 102);
+      for (int i = 0; i < C::NSTAGE; ++i)
+        if (used_mask >> i & 1u) mbar_wait(&bar_qdo_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 103);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, BQ, 0, 0);        // S^T, dP^T
+      const uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);         // dV, dK (B = dO / Q, MN-major)
+      const uint32_t idesc_q = C::DQ_TRANSPOSED ? idesc_bf16_f32(128, BQ, 1, 1)   // dQ^T = K^T dS^T
+                                                : idesc_bf16_f32(128, D, 1, 1);   // dQ = dS K
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      bool ok = mbar_wait(bar_kv, 0, abort_flag, p.status, 110);
+      tc_fence_after();
+
+      auto first_half = [&](int st) -> bool {  // S^T, dP^T of step st
+        const int slot = st % C::NSTAGE, buf = st % C::NBUF;
+        if (!mbar_wait(&bar_qdo_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 111)) return false;
+        if (st >= C::NBUF && !mbar_wait(&bar_dq_free[buf], ((st - C::NBUF) / C::NBUF) & 1, abort_flag, p.status, 112))
+          return false;
+        tc_fence_after();
+        const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
+        const uint32_t sdo = sq + C::Q_TILE;
+        const uint32_t tb = tmem + buf * C::BUF_COLS;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k / 4) * C::KV_BOX + (k % 4) * 32;
+          const uint32_t qoff = (k / 4) * C::QBOX + (k % 4) * 32;
+          mma_ss(tb, smem_desc_sw128(sK + koff, 16, 1024), smem_desc_sw128(sq + qoff, 16, 1024), idesc_s, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k / 4) * C::KV_BOX + (k % 4) * 32;
+          const uint32_t qoff = (k / 4) * C::QBOX + (k % 4) * 32;
+          mma_ss(tb + BQ, smem_desc_sw128(sV + koff, 16, 1024), smem_desc_sw128(sdo + qoff, 16, 1024), idesc_s,
+                 k > 0);
+        }
+        mma_commit(&bar_sdp_full[buf]);
+        return true;
+      };
+      auto second_half = [&](int st) -> bool {  // dV, dK, dQ of step st
+        const int slot = st % C::NSTAGE, buf = st % C::NBUF, dsb = st & 1;
+        if (!mbar_wait(&bar_p_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 113)) return false;
+        tc_fence_after();
+        const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
+        const uint32_t sdo = sq + C::Q_TILE;
+        const uint32_t tb = tmem + buf * C::BUF_COLS;
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + C::DV_COL, tb + C::P_COL + k * 8, smem_desc_sw128(sdo + k * 2048, C::QBOX, 1024), idesc_g,
+                 (st > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + C::DK_COL, tb + C::DS_COL + k * 8, smem_desc_sw128(sq + k * 2048, C::QBOX, 1024), idesc_g,
+                 (st > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar_qdo_empty[slot]);
+        const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {
+          if (C::DQ_TRANSPOSED)
+            mma_ss(tb + C::DQ_COL, smem_desc_sw128(sK + k * 2048, C::KV_BOX, 1024),
+                   smem_desc_sw128(sds + k * 2048, C::DS_BLOCK, 1024), idesc_q, k > 0);
+          else
+            mma_ss(tb + C::DQ_COL, smem_desc_sw128(sds + k * 2048, C::DS_BLOCK, 1024),
+                   smem_desc_sw128(sK + k * 2048, C::KV_BOX, 1024), idesc_q, k > 0);
+        }
+        mma_commit(&bar_dq_full[buf]);
+        mma_commit(&bar_ds_free[dsb]);
+        return true;
+      };
+
+      StepIter it;
+      it.init(G, s.Sq, BQ, ibeg);
+      int n = 0;
+      for (; ok && it.valid(); it.next()) {
+        if (step_skipped(it)) continue;
+        if (C::NBUF == 1) {
+          if (n > 0 && !(ok = second_half(n - 1))) break;
+          if (!(ok = first_half(n))) break;
+        } else {
+          if (!(ok = first_half(n))) break;
+          if (n > 0 && !(ok = second_half(n - 1))) break;
+        }
+        ++n;
+      }
+      if (ok && n > 0) ok = second_half(n - 1);
+      mma_commit(bar_mma_done);
+      mbar_wait(bar_mma_done, 0, nullptr, p.status, 114);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- LSE / D staging
+    StepIter it;
+    it.init(G, s.Sq, BQ, ibeg);
+    const float l2e = kLog2e;
+    for (int st = 0; it.valid(); it.next()) {
+      if (step_skipped(it)) continue;
+      const int slot = st % C::NSTAGE;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_lsed_empty[slot], ((st / C::NSTAGE) & 1) ^ 1, abort_flag, p.status,
+                                              120)))
+        break;
+      const size_t rowbase = (size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq;
+      float* dst = lsed + slot * 2 * BQ;
+#pragma unroll
+      for (int r = lane; r < BQ; r += 32) {
+        const int i = it.i0 + r;
+        const bool in = i < s.Sq;
+        dst[r] = in ? p.lse[rowbase + i] * l2e : 0.f;
+        dst[BQ + r] = in ? p.dsum[rowbase + i] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_lsed_full[slot]);
+      ++st;
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------------- softmax-grad: a thread owns key j
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int j = j0 + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = s.scale * kLog2e;
+    const bool key_ok = j < s.Sk;
+    StepIter it;
+    it.init(G, s.Sq, BQ, ibeg);
+    int st = 0;
+    bool ok = true;
+    for (; it.valid(); it.next()) {
+      if (step_skipped(it)) continue;
+      const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st & 1;
+      ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
+      ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
+      if (st >= 2) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - 2) / 2) & 1, abort_flag, p.status, 132);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
+      const float* lse2 = lsed + slot * 2 * BQ;
+      const float* dsv = lse2 + BQ;
+      const int code = bwd_tile_code(p, mb, it.i0, kt);
+      const size_t mrow0 = (size_t)mb * s.Sq;
+      // whole step visible for this key: open tile, all rows real, causal rule satisfied by the first row
+      const bool full = code == TILE_OPEN && key_ok && it.i0 + BQ <= s.Sq &&
+                        (!s.causal || (long long)j <= s.q_offset + it.i0);
+      const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE) + r * 128;
+      uint32_t dpend[16];  // dS^T of the previous chunk, written one chunk late (its TMEM columns
+                           // hold scores that are read only in the next chunk)
+#pragma unroll
+      for (int c = 0; c < BQ / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tb + c * 32, sr);
+        tmem_ld32(tb + BQ + c * 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+        if (c > 0) tmem_st16(tb + C::DS_COL + (c - 1) * 16, dpend);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int q = c * 32 + e + u;
+            const int i = it.i0 + q;
+            float x = __uint_as_float(sr[e + u]);
+            bool vis = true;
+            float bias = 0.f;
+            if (!full) {
+              vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
+              if (vis && code == TILE_MIXED) {
+                const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
+                if (s.mask_kind == MK_ADD) {
+                  const float mv = static_cast<const float*>(p.mask)[midx];
+                  vis = mv > kMaskFloor;
+                  bias = mv * kLog2e;
+                } else {
+                  vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
+                }
+              }
+            }
+            const float pv = vis ? ex2_approx(fmaf(x, sl2, bias) - lse2[q]) : 0.f;
+            pp[u] = pv;
+            dd[u] = pv * (__uint_as_float(dr[e + u]) - dsv[q]);
+          }
+          pk[e / 2] = pack_bf16x2(pp[0], pp[1]);
+          dpend[e / 2] = pack_bf16x2(dd[0], dd[1]);
+        }
+        tmem_st16(tb + C::P_COL + c * 16, pk);
+        // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (4 x 16 B chunks per 32 queries)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = c * 4 + u;              // 16-byte chunk among the BQ / 8 of this row
+          const int blk = chunk / 8, cin = chunk % 8;
+          st_shared_v4(sds + blk * C::DS_BLOCK + ((cin ^ (r & 7)) * 16), dpend[4 * u], dpend[4 * u + 1],
+                       dpend[4 * u + 2], dpend[4 * u + 3]);
+        }
+      }
+      tmem_st16(tb + C::DS_COL + (BQ / 32 - 1) * 16, dpend);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_p_full[buf]);
+        mbar_arrive(&bar_lsed_empty[slot]);
+      }
+      ++st;
+    }
+    // ---- epilogue: dV and scale * dK of this thread's key, from TMEM
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && st > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma_done, 0, abort_flag, p.status, 133));
+    tc_fence_after();
+    if (ok) {
+      const size_t row = ((size_t)(b * s.Hkv + kvh) * s.Sk + (key_ok ? j : 0)) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which == 0 ? 1.f : s.scale;
+        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
+        void* outp = which == 0 ? p.dv : p.dk;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          if (st > 0) {
+            tmem_ld32(tcol + c * 32, v);
+            tmem_wait_ld();
+            reg_fence(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          if (!key_ok) continue;
+          if (p.accum) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(outp) + row + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 a = dst[v4];
+              a.x += __uint_as_float(v[4 * v4]) * mul;
+              a.y += __uint_as_float(v[4 * v4 + 1]) * mul;
+              a.z += __uint_as_float(v[4 * v4 + 2]) * mul;
+              a.w += __uint_as_float(v[4 * v4 + 3]) * mul;
+              dst[v4] = a;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outp) + row + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                w[u] = pack_bf16x2(__uint_as_float(v[8 * v4 + 2 * u]) * mul, __uint_as_float(v[8 * v4 + 2 * u + 1]) * mul);
+              dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------- dQ writer
+    const int wq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    StepIter it;
+    it.init(G, s.Sq, BQ, ibeg);
+    int st = 0;
+    for (; it.valid(); it.next()) {
+      if (step_skipped(it)) continue;
+      const int buf = st % C::NBUF;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 140)))
+        break;
+      tc_fence_after();
+      const uint32_t tq = tmem + buf * C::BUF_COLS + C::DQ_COL + lane_off;
+      constexpr int NC = C::DQ_TRANSPOSED ? BQ / 32 : D / 32;
+      uint32_t v[NC][32];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) tmem_ld32(tq + c * 32, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < NC; ++c) reg_fence(v[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
+      const size_t rowbase = (size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq;
+      if (C::DQ_TRANSPOSED) {
+        // thread = feature d; column q = query row i0 + q: lanes cover 32 consecutive d of one row
+        const int d = wq * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = it.i0 + c * 32 + e;
+            if (i < s.Sq) atomicAdd(p.dq_acc + (rowbase + i) * D + d, __uint_as_float(v[c][e]));
+          }
+      } else {
+        // thread = query row; columns = features
+        const int i = it.i0 + wq * 32 + lane;
+        if (i < s.Sq) {
+          float* dst = p.dq_acc + (rowbase + i) * D;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) atomicAdd(dst + c * 32 + e, __uint_as_float(v[c][e]));
+        }
+      }
+      ++st;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool tc_bwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq > 0; }
+
+template <int D>
+static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, unsigned* status) {
+  using C = BwdCfg<D>;
+  const Shape& s = a.s;
+  BwdTcParams p;
+  cudaError_t e;
+  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_do, a.dO, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  p.s = s;
+  p.mask = a.mask;
+  p.nqt = (s.Sq + 127) / 128;
+  p.nkt = (s.Sk + kBN - 1) / kBN;
+  p.tilemap = nullptr;
+  if (s.mask_kind != MK_NONE) {
+    uint8_t* tm = reinterpret_cast<uint8_t*>(ws + plan.tilemap_off);
+    if ((e = launch_mask_classify(s, a.mask, tm, a.stream)) != cudaSuccess) return e;
+    p.tilemap = tm;
+  }
+  float* dsum = reinterpret_cast<float*>(ws + plan.dsum_off);
+  float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
+  if ((e = launch_dsum(a, dsum, dq_acc)) != cudaSuccess) return e;
+  p.lse = a.lse;
+  p.dsum = dsum;
+  p.dq_acc = dq_acc;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.accum = a.accum ? 1 : 0;
+  p.status = status;
+  const int smem = C::BYTES;
+  if ((e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  const long long ctas = (long long)s.B * s.Hkv * p.nkt;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if ((e = prof_begin(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
+  bwd_tc_kernel<D><<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = prof_end(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
+  return launch_dq_convert(a, dq_acc);
+}
+
+cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws) {
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorUnknown;
+  return a.s.D == 64 ? tc_bwd_t<64>(a, plan, ws, status) : tc_bwd_t<128>(a, plan, ws, status);
+}
+
+}  // namespace fa

@@ -490,8 +490,8 @@ int kv_tiles_total(const Shape& s) {
 
 }  // namespace
 
-// bf16 [rows-of-D] tensor viewed as (D, S, heads), boxes of 64 x 128 x 1 with 128-byte swizzle.
-cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D) {
+// bf16 [heads, S, D] tensor viewed as (D, S, heads), boxes of 64 x box_rows x 1 with 128-byte swizzle.
+cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
   static EncodeTiledFn encode = nullptr;
   if (encode == nullptr) {
     cudaDriverEntryPointQueryResult q;
@@ -502,7 +502,7 @@ cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads,
   }
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -525,9 +525,9 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   const Shape& s = a.s;
   FwdTcParams p;
   cudaError_t e;
-  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D, kBM)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + kBM - 1) / kBM;

@@ -288,6 +288,12 @@ def run_ours(args):
     step_ev = [(ev(), ev()) for _ in range(K)]
     kern = {kid: [(ev(), ev()) for _ in range(K)] for kid in (ft.FA_KERNEL_FWD, ft.FA_KERNEL_BWD_MAIN,
                                                               ft.FA_KERNEL_BWD_DSUM, ft.FA_KERNEL_BWD_DQ_CONVERT)}
+    # torch creates the CUDA event lazily at its first record(): materialise every handle
+    # before the library is asked to record it
+    for evs in kern.values():
+        for a_, b_ in evs:
+            a_.record()
+            b_.record()
     barrier(world)
     torch.cuda.synchronize()
     launches0 = ft.profile_launch_count()
