@@ -9,7 +9,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/fa_train.h"
+#include "fa_train.h"
 #include "fa_internal.h"
 
 namespace fa {

@@ -336,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
-      const float* lse2 = lsed + slot * 2 * BQ;
-      const float* dsv = lse2 + BQ;
+      const uint32_t lse_s = smem_u32(lsed + slot * 2 * BQ);  // [lse * log2(e) x BQ | D x BQ]
       const int code = bwd_tile_code(p, mb, it.i0, kt);
       const size_t mrow0 = (size_t)mb * s.Sq;
       // whole step visible for this key: open tile, all rows real, causal rule satisfied by the first row
@@ -355,36 +354,44 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         reg_fence(sr);
         reg_fence(dr);
         if (c > 0) tmem_st16(tb + C::DS_COL + (c - 1) * 16, dpend);
-        uint32_t pk[16];
+        // this chunk's 32 query rows: LSE * log2(e) and D, straight from shared memory
+        float l2[32], dv_[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pp[2], dd[2];
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 a = ld_shared_f4(lse_s + (c * 32 + 4 * v4) * 4);
+          const float4 d = ld_shared_f4(lse_s + (BQ + c * 32 + 4 * v4) * 4);
+          l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
+          dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
+        }
+        float pv[32];
+        if (full) {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int q = c * 32 + e + u;
-            const int i = it.i0 + q;
-            float x = __uint_as_float(sr[e + u]);
-            bool vis = true;
+          for (int e = 0; e < 32; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -l2[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = it.i0 + c * 32 + e;
+            bool vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
             float bias = 0.f;
-            if (!full) {
-              vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
-              if (vis && code == TILE_MIXED) {
-                const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
-                if (s.mask_kind == MK_ADD) {
-                  const float mv = static_cast<const float*>(p.mask)[midx];
-                  vis = mv > kMaskFloor;
-                  bias = mv * kLog2e;
-                } else {
-                  vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
-                }
+            if (vis && code == TILE_MIXED) {
+              const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
+              if (s.mask_kind == MK_ADD) {
+                const float mv = static_cast<const float*>(p.mask)[midx];
+                vis = mv > kMaskFloor;
+                bias = mv * kLog2e;
+              } else {
+                vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
               }
             }
-            const float pv = vis ? ex2_approx(fmaf(x, sl2, bias) - lse2[q]) : 0.f;
-            pp[u] = pv;
-            dd[u] = pv * (__uint_as_float(dr[e + u]) - dsv[q]);
+            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, bias - l2[e])) : 0.f;
           }
-          pk[e / 2] = pack_bf16x2(pp[0], pp[1]);
-          dpend[e / 2] = pack_bf16x2(dd[0], dd[1]);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+          dpend[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
+                                 pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
         }
         tmem_st16(tb + C::P_COL + c * 16, pk);
         // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (4 x 16 B chunks per 32 queries)

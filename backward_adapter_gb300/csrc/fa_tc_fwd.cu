@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       };
       // pass 1: row max of this tile
       // (TMEM loads and stores are warp-collective: every lane issues them, hidden rows just get -inf)
-      float tmax = -CUDART_INF_F;
+      float tm4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};  // 4 independent chains
 #pragma unroll
       for (int cch = 0; cch < kBN / 32; ++cch) {
         uint32_t raw[32];
@@ -318,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         reg_fence(raw);
         masked(raw, cch * 32, x);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, x[e]);
+        for (int e = 0; e < 32; ++e) tm4[e & 3] = fmaxf(tm4[e & 3], x[e]);
       }
+      const float tmax = fmaxf(fmaxf(tm4[0], tm4[1]), fmaxf(tm4[2], tm4[3]));
       const float m_new = fmaxf(m, tmax);
       const bool rescale = m_new > m + kRescaleThreshold;   // false while nothing is visible
       const float m_use = rescale ? m_new : m;
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
       // pass 2: P = 2^(x - m) as bf16 over the first 64 columns of the score block; chunk c of
       // the scores is read before P chunk c lands on columns [16c, 16c + 16) (already read)
-      float sum = 0.f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cch = 0; cch < kBN / 32; ++cch) {
         uint32_t pk[16];
@@ -341,11 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2_approx(x[2 * e] - m_sub);
           const float p1 = ex2_approx(x[2 * e + 1] - m_sub);
-          sum += p0 + p1;
+          sum4[e & 3] += p0 + p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + cch * 16, pk);
       }
+      const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       l = l * alpha + sum;
       m = m_use;
       if (__any_sync(0xffffffffu, rescale) && idx > 0) {  // alpha = 1 on rows that keep their max
