@@ -94,6 +94,7 @@ cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tile
 bool tc_fwd_supported(const Shape& s);
 bool tc_bwd_supported(const Shape& s);
 cudaError_t make_tmap_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D, int box_rows);
+cudaError_t make_tmap_f32_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D, int box_rows);
 int tc_fwd_kv_splits(const Shape& s);
 cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);
 cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws);

@@ -17,12 +17,16 @@
 //     dV  += P^T dO          (TMEM x SMEM)
 //     dK  += dS^T Q          (TMEM x SMEM)
 //     dQ^T = K^T dS^T  (D = 128)  or  dQ = dS K  (D = 64)   (SMEM x SMEM -> TMEM)
-//     dQ writer warps add the dQ partial into the fp32 dQ accumulator (red.add).
+//     the dQ partial goes TMEM -> SMEM -> fp32 dQ accumulator with one TMA bulk
+//     tensor reduce-add (the add happens in L2).
 // Roles: warp 0 TMA (K, V once; Q, dO per step), warp 1 MMA issue + TMEM owner,
-// warp 2 LSE/D staging, warps 4-7 softmax-grad (a thread owns one key),
-// warps 8-11 dQ writer. With D = 128 the S/dP TMEM block is double-buffered so
-// the next step's S^T, dP^T run on the tensor core while the softmax-grad warps
-// work on the current one.
+// warp 2 LSE/D staging, warps 4-11 softmax-grad: two warps per TMEM lane quadrant,
+// a thread owns one key and half of the step's query columns; after the scores
+// of step n they also stage the dQ partial of step n-1. Each 32-column score
+// chunk receives its own P^T (16 columns) and dS^T (16 columns) once read, so no
+// warp writes TMEM another warp still reads. With D = 128 the S/dP TMEM block is
+// double-buffered so the next step's S^T, dP^T run on the tensor core while the
+// softmax-grad warps work on the current one.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,13 +49,15 @@ struct BwdCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;        // query rows per step
   static constexpr int NBUF = D == 128 ? 2 : 1;         // S/dP TMEM blocks
   static constexpr int BUF_COLS = 2 * BQ;               // S^T [0,BQ), dP^T [BQ,2BQ)
-  static constexpr int P_COL = 0;                       // P^T (bf16) over the first BQ/2 columns
-  static constexpr int DS_COL = D == 128 ? 32 : 128;    // dS^T (bf16)
-  static constexpr int DQ_COL = D == 128 ? 64 : 64;     // dQ^T (D=128: 64 cols) / dQ (D=64: 64 cols)
+  static constexpr int NCHUNK = BQ / 32;                // 32-column score chunks per step
+  static constexpr int CHUNKS_PER_WARP = NCHUNK / 2;    // two warps per lane quadrant
+  // chunk c of the scores (columns [32c, 32c+32)) is overwritten by P^T at [32c, 32c+16)
+  // and dS^T at [32c+16, 32c+32) (bf16 pairs) once it has been read
+  static constexpr int DQ_COL = BQ;                     // dQ^T (D=128) / dQ (D=64) over the dP^T block
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
   static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
-  static constexpr int NSTAGE = 3;                      // Q/dO ring depth
+  static constexpr int NSTAGE = 2;                      // Q/dO ring depth
   // shared memory (bytes)
   static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
   static constexpr int KV_TILE = kBN * D * 2;
@@ -59,17 +65,20 @@ struct BwdCfg {
   static constexpr int Q_TILE = BQ * D * 2;
   static constexpr int DS_BLOCK = 128 * 128;            // 128 keys x 64 queries (bf16)
   static constexpr int DS_TILE = (BQ / 64) * DS_BLOCK;
+  static constexpr int DQ_STAGE = BQ * D * 4;           // fp32 [BQ][D] staging of the dQ partial
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_STAGE = 2 * KV_TILE;         // [NSTAGE] x (Q, dO)
   static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // [2] x dS^T
-  static constexpr int OFF_LSED = OFF_DS + 2 * DS_TILE;            // [NSTAGE] x (lse2[BQ], dsum[BQ])
+  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;              // dQ staging
+  static constexpr int OFF_LSED = OFF_DQ + DQ_STAGE;               // [NSTAGE] x (lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
   static constexpr int BYTES = OFF_BAR + 512 + 1024;
+  static constexpr int SM_THREADS = 256;                // softmax-grad warps 4..11
 };
 
 struct BwdTcParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
   Shape s;
   const void* mask;
   const uint8_t* tilemap;
@@ -121,7 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
   uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 2
   uint64_t* bar_mma_done = bar_ds_free + 2;             // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
+  uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 8 softmax-grad warps filled the dQ staging
+  uint64_t* bar_stage_free = bar_stage_full + 1;        // 1: the previous reduce finished reading it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_stage_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* lsed = reinterpret_cast<float*>(smem + C::OFF_LSED);
 
@@ -147,17 +158,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_qdo_full[i], 1);
       mbar_init(&bar_qdo_empty[i], 1);
       mbar_init(&bar_lsed_full[i], 1);
-      mbar_init(&bar_lsed_empty[i], 4);
+      mbar_init(&bar_lsed_empty[i], 8);
     }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&bar_sdp_full[i], 1);
-      mbar_init(&bar_p_full[i], 4);
+      mbar_init(&bar_p_full[i], 8);
       mbar_init(&bar_dq_full[i], 1);
-      mbar_init(&bar_dq_free[i], 4);
+      mbar_init(&bar_dq_free[i], 8);
     }
     mbar_init(&bar_ds_free[0], 1);
     mbar_init(&bar_ds_free[1], 1);
     mbar_init(bar_mma_done, 1);
+    mbar_init(bar_stage_full, 8);
+    mbar_init(bar_stage_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -176,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       prefetch_tmap(&p.tm_k);
       prefetch_tmap(&p.tm_v);
       prefetch_tmap(&p.tm_do);
+      prefetch_tmap(&p.tm_dq);
       const int kvrow = b * s.Hkv + kvh;
       mbar_arrive_expect_tx(bar_kv, 2 * C::KV_TILE);
       for (int box = 0; box < D / 64; ++box) {
@@ -249,14 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint32_t sdo = sq + C::Q_TILE;
         const uint32_t tb = tmem + buf * C::BUF_COLS;
+        // k-step k covers queries [16k, 16k+16): chunk k/2, columns (k%2)*8 within its P^T / dS^T half
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DV_COL, tb + C::P_COL + k * 8, smem_desc_sw128(sdo + k * 2048, C::QBOX, 1024), idesc_g,
-                 (st > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, tb + 32 * (k / 2) + (k % 2) * 8, smem_desc_sw128(sdo + k * 2048, C::QBOX, 1024),
+                 idesc_g, (st > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DK_COL, tb + C::DS_COL + k * 8, smem_desc_sw128(sq + k * 2048, C::QBOX, 1024), idesc_g,
-                 (st > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tb + 32 * (k / 2) + 16 + (k % 2) * 8,
+                 smem_desc_sw128(sq + k * 2048, C::QBOX, 1024), idesc_g, (st > 0 || k > 0) ? 1u : 0u);
         mma_commit(&bar_qdo_empty[slot]);
         const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE);
 #pragma unroll
@@ -315,21 +330,79 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&bar_lsed_full[slot]);
       ++st;
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------------- softmax-grad: a thread owns key j
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax-grad + dQ staging
+    const int wq = warp & 3;                      // TMEM lane quadrant
+    const int half = (warp - 4) >> 2;             // which half of the step's query columns
+    const int r = wq * 32 + lane;                 // key row within the tile
     const int j = j0 + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = s.scale * kLog2e;
     const bool key_ok = j < s.Sk;
+    const bool leader = threadIdx.x == 128;       // issues the dQ bulk reductions
+    const size_t mrow0 = (size_t)mb * s.Sq;
+    float* sdq = reinterpret_cast<float*>(smem + C::OFF_DQ);
+
+    // dQ partial of finished step st (the round-th staging): TMEM -> SMEM [BQ][D] fp32 -> dQ accumulator
+    // with one TMA reduce-add issued by the leader thread
+    auto stage_dq = [&](int st, int round, int i0, int hh) -> bool {
+      const int buf = st % C::NBUF;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134));
+      if (!ok) return false;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + half * 32 + lane_off, v);
+      tmem_wait_ld();
+      reg_fence(v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
+      if (round > 0) {
+        // the previous reduce-add must have finished reading the staging buffer
+        if (leader) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar_stage_free);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_stage_free, (round - 1) & 1, abort_flag, p.status, 135));
+        if (!ok) return false;
+      }
+      const uint32_t sbase = smem_u32(sdq);
+      if (C::DQ_TRANSPOSED) {
+        // thread = feature d, registers = queries 32*half + e: row-major [q][d] stores, lanes on consecutive d
+        const int d = wq * 32 + lane;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((half * 32 + e) * D + d) * 4, __uint_as_float(v[e]));
+      } else {
+        // thread = query row, registers = features 32*half + e; 16-byte chunks rotated across lanes
+        const int q = wq * 32 + lane;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int cidx = (u + lane) & 7;
+          st_shared_v4(sbase + (q * D + half * 32 + 4 * cidx) * 4, v[4 * cidx], v[4 * cidx + 1], v[4 * cidx + 2],
+                       v[4 * cidx + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_stage_full);
+      if (leader) {
+        if (!mbar_wait(bar_stage_full, round & 1, abort_flag, p.status, 136)) return false;
+        tma_reduce_add_3d(&p.tm_dq, sdq, 0, i0, b * s.Hq + kvh * G + hh);
+        bulk_commit_group();
+      }
+      return true;
+    };
+
     StepIter it;
     it.init(G, s.Sq, BQ, ibeg);
-    int st = 0;
+    int st = 0, prev_i0 = 0, prev_hh = 0;
     bool ok = true;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
       const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st & 1;
+      // one S/dP block: this step's S^T overwrites the block holding the previous dQ partial,
+      // so that partial is staged first (with two blocks it is staged after this step's P)
+      if (C::NBUF == 1 && st > 0 && !(ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh))) break;
       ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
       if (st >= 2) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - 2) / 2) & 1, abort_flag, p.status, 132);
@@ -338,23 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
       const uint32_t lse_s = smem_u32(lsed + slot * 2 * BQ);  // [lse * log2(e) x BQ | D x BQ]
       const int code = bwd_tile_code(p, mb, it.i0, kt);
-      const size_t mrow0 = (size_t)mb * s.Sq;
-      // whole step visible for this key: open tile, all rows real, causal rule satisfied by the first row
+      // every pair of this step visible for this key: open tile, real rows, causal rule met by the first row
       const bool full = code == TILE_OPEN && key_ok && it.i0 + BQ <= s.Sq &&
                         (!s.causal || (long long)j <= s.q_offset + it.i0);
       const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE) + r * 128;
-      uint32_t dpend[16];  // dS^T of the previous chunk, written one chunk late (its TMEM columns
-                           // hold scores that are read only in the next chunk)
 #pragma unroll
-      for (int c = 0; c < BQ / 32; ++c) {
+      for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
+        const int c = half * C::CHUNKS_PER_WARP + cc;   // score chunk: queries [32c, 32c+32)
         uint32_t sr[32], dr[32];
         tmem_ld32(tb + c * 32, sr);
         tmem_ld32(tb + BQ + c * 32, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-        if (c > 0) tmem_st16(tb + C::DS_COL + (c - 1) * 16, dpend);
-        // this chunk's 32 query rows: LSE * log2(e) and D, straight from shared memory
         float l2[32], dv_[32];
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4) {
@@ -363,6 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
           dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
         }
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
         float pv[32];
         if (full) {
 #pragma unroll
@@ -386,24 +455,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, bias - l2[e])) : 0.f;
           }
         }
-        uint32_t pk[16];
+        uint32_t pk[16], dk16[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          dpend[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
-                                 pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
+          dk16[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
+                                pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
         }
-        tmem_st16(tb + C::P_COL + c * 16, pk);
+        // P^T and dS^T of these 32 queries over this chunk's own (already read) score columns
+        tmem_st16(tb + c * 32, pk);
+        tmem_st16(tb + c * 32 + 16, dk16);
         // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (4 x 16 B chunks per 32 queries)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int chunk = c * 4 + u;              // 16-byte chunk among the BQ / 8 of this row
           const int blk = chunk / 8, cin = chunk % 8;
-          st_shared_v4(sds + blk * C::DS_BLOCK + ((cin ^ (r & 7)) * 16), dpend[4 * u], dpend[4 * u + 1],
-                       dpend[4 * u + 2], dpend[4 * u + 3]);
+          st_shared_v4(sds + blk * C::DS_BLOCK + ((cin ^ (r & 7)) * 16), dk16[4 * u], dk16[4 * u + 1],
+                       dk16[4 * u + 2], dk16[4 * u + 3]);
         }
       }
-      tmem_st16(tb + C::DS_COL + (BQ / 32 - 1) * 16, dpend);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -412,9 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_arrive(&bar_p_full[buf]);
         mbar_arrive(&bar_lsed_empty[slot]);
       }
+      // the dQ partial of the previous step is ready by now (its MMA was issued before this step's P)
+      if (C::NBUF == 2 && st > 0 && !(ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh))) break;
+      prev_i0 = it.i0;
+      prev_hh = it.hh;
       ++st;
     }
-    // ---- epilogue: dV and scale * dK of this thread's key, from TMEM
+    if (ok && st > 0) ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh);
+    if (leader) bulk_wait_group0();
+    // ---- epilogue: dV and scale * dK of this thread's key, from TMEM; each warp of the
+    //      quadrant pair takes half of the feature columns
     ok = __all_sync(0xffffffffu, ok);
     if (ok && st > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma_done, 0, abort_flag, p.status, 133));
     tc_fence_after();
@@ -426,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
         void* outp = which == 0 ? p.dv : p.dk;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = half * (D / 64) + cc;      // 32-feature chunk
           uint32_t v[32];
           if (st > 0) {
             tmem_ld32(tcol + c * 32, v);
@@ -462,54 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
       }
     }
-  } else if (warp >= 8) {
-    // ---------------------------------------------------------------- dQ writer
-    const int wq = warp & 3;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    StepIter it;
-    it.init(G, s.Sq, BQ, ibeg);
-    int st = 0;
-    for (; it.valid(); it.next()) {
-      if (step_skipped(it)) continue;
-      const int buf = st % C::NBUF;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 140)))
-        break;
-      tc_fence_after();
-      const uint32_t tq = tmem + buf * C::BUF_COLS + C::DQ_COL + lane_off;
-      constexpr int NC = C::DQ_TRANSPOSED ? BQ / 32 : D / 32;
-      uint32_t v[NC][32];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) tmem_ld32(tq + c * 32, v[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < NC; ++c) reg_fence(v[c]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
-      const size_t rowbase = (size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq;
-      if (C::DQ_TRANSPOSED) {
-        // thread = feature d; column q = query row i0 + q: lanes cover 32 consecutive d of one row
-        const int d = wq * 32 + lane;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = it.i0 + c * 32 + e;
-            if (i < s.Sq) atomicAdd(p.dq_acc + (rowbase + i) * D + d, __uint_as_float(v[c][e]));
-          }
-      } else {
-        // thread = query row; columns = features
-        const int i = it.i0 + wq * 32 + lane;
-        if (i < s.Sq) {
-          float* dst = p.dq_acc + (rowbase + i) * D;
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) atomicAdd(dst + c * 32 + e, __uint_as_float(v[c][e]));
-        }
-      }
-      ++st;
-    }
   }
 
   tc_fence_before();
@@ -534,6 +564,8 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   if ((e = make_tmap_bhsd(&p.tm_do, a.dO, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
   if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
   if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
+  if ((e = make_tmap_f32_bhsd(&p.tm_dq, dq_acc, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + 127) / 128;
@@ -545,7 +577,6 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.tilemap = tm;
   }
   float* dsum = reinterpret_cast<float*>(ws + plan.dsum_off);
-  float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
   if ((e = launch_dsum(a, dsum, dq_acc)) != cudaSuccess) return e;
   p.lse = a.lse;
   p.dsum = dsum;

@@ -492,22 +492,42 @@ int kv_tiles_total(const Shape& s) {
 
 }  // namespace
 
-// bf16 [heads, S, D] tensor viewed as (D, S, heads), boxes of 64 x box_rows x 1 with 128-byte swizzle.
-cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
+static EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn encode = nullptr;
   if (encode == nullptr) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return nullptr;
     encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
+  return encode;
+}
+
+// bf16 [heads, S, D] tensor viewed as (D, S, heads), boxes of 64 x box_rows x 1 with 128-byte swizzle.
+cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// fp32 [heads, S, D] tensor viewed as (D, S, heads), unswizzled boxes of D x box_rows x 1.
+cudaError_t make_tmap_f32_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)S * D * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

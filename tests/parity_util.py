@@ -39,7 +39,8 @@ def run_gpu(w: wl.Workload, t: dict) -> dict:
     else:
         dq, dk, dv = ft.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], t["mask"], **kw)
     torch.cuda.synchronize()
-    assert ft.device_status() == 0, "a bounded wait inside a kernel ran out of time"
+    status = ft.device_status()
+    assert status == 0, f"a bounded wait inside a kernel ran out of time (site {status & 0xffff})"
     return {n: x.double().cpu().numpy() for n, x in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
 
 
