@@ -21,8 +21,8 @@
 //     tensor reduce-add (the add happens in L2).
 // Roles: warp 0 TMA (K, V once; Q, dO per step), warp 1 MMA issue + TMEM owner,
 // warp 2 LSE/D staging, warps 4-11 softmax-grad: two warps per TMEM lane quadrant,
-// a thread owns one key and half of the step's query columns; after the scores
-// of step n they also stage the dQ partial of step n-1. Each 32-column score
+// a thread owns one key and half of the step's query columns; warps 12-15 stage
+// each step's dQ partial (TMEM -> SMEM) and issue its reduce-add. Each 32-column score
 // chunk receives its own P^T (16 columns) and dS^T (16 columns) once read, so no
 // warp writes TMEM another warp still reads. With D = 128 the S/dP TMEM block is
 // double-buffered so the next step's S^T, dP^T run on the tensor core while the
@@ -41,7 +41,7 @@ namespace {
 using namespace tc;
 
 constexpr int kBN = 128;       // keys per CTA
-constexpr int kThreads = 384;  // 12 warps
+constexpr int kThreads = 512;  // 16 warps = 4 warpgroups (128 registers per thread)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -74,7 +74,6 @@ struct BwdCfg {
   static constexpr int OFF_LSED = OFF_DQ + DQ_STAGE;               // [NSTAGE] x (lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
   static constexpr int BYTES = OFF_BAR + 512 + 1024;
-  static constexpr int SM_THREADS = 256;                // softmax-grad warps 4..11
 };
 
 struct BwdTcParams {
@@ -164,12 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_sdp_full[i], 1);
       mbar_init(&bar_p_full[i], 8);
       mbar_init(&bar_dq_full[i], 1);
-      mbar_init(&bar_dq_free[i], 8);
+      mbar_init(&bar_dq_free[i], 4);
     }
     mbar_init(&bar_ds_free[0], 1);
     mbar_init(&bar_ds_free[1], 1);
     mbar_init(bar_mma_done, 1);
-    mbar_init(bar_stage_full, 8);
+    mbar_init(bar_stage_full, 4);
     mbar_init(bar_stage_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -330,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&bar_lsed_full[slot]);
       ++st;
     }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------------- softmax-grad + dQ staging
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------------- softmax-grad
     const int wq = warp & 3;                      // TMEM lane quadrant
     const int half = (warp - 4) >> 2;             // which half of the step's query columns
     const int r = wq * 32 + lane;                 // key row within the tile
@@ -339,70 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = s.scale * kLog2e;
     const bool key_ok = j < s.Sk;
-    const bool leader = threadIdx.x == 128;       // issues the dQ bulk reductions
     const size_t mrow0 = (size_t)mb * s.Sq;
-    float* sdq = reinterpret_cast<float*>(smem + C::OFF_DQ);
-
-    // dQ partial of finished step st (the round-th staging): TMEM -> SMEM [BQ][D] fp32 -> dQ accumulator
-    // with one TMA reduce-add issued by the leader thread
-    auto stage_dq = [&](int st, int round, int i0, int hh) -> bool {
-      const int buf = st % C::NBUF;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134));
-      if (!ok) return false;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + half * 32 + lane_off, v);
-      tmem_wait_ld();
-      reg_fence(v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
-      if (round > 0) {
-        // the previous reduce-add must have finished reading the staging buffer
-        if (leader) {
-          bulk_wait_group_read0();
-          mbar_arrive(bar_stage_free);
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_stage_free, (round - 1) & 1, abort_flag, p.status, 135));
-        if (!ok) return false;
-      }
-      const uint32_t sbase = smem_u32(sdq);
-      if (C::DQ_TRANSPOSED) {
-        // thread = feature d, registers = queries 32*half + e: row-major [q][d] stores, lanes on consecutive d
-        const int d = wq * 32 + lane;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((half * 32 + e) * D + d) * 4, __uint_as_float(v[e]));
-      } else {
-        // thread = query row, registers = features 32*half + e; 16-byte chunks rotated across lanes
-        const int q = wq * 32 + lane;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int cidx = (u + lane) & 7;
-          st_shared_v4(sbase + (q * D + half * 32 + 4 * cidx) * 4, v[4 * cidx], v[4 * cidx + 1], v[4 * cidx + 2],
-                       v[4 * cidx + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_stage_full);
-      if (leader) {
-        if (!mbar_wait(bar_stage_full, round & 1, abort_flag, p.status, 136)) return false;
-        tma_reduce_add_3d(&p.tm_dq, sdq, 0, i0, b * s.Hq + kvh * G + hh);
-        bulk_commit_group();
-      }
-      return true;
-    };
 
     StepIter it;
     it.init(G, s.Sq, BQ, ibeg);
-    int st = 0, prev_i0 = 0, prev_hh = 0;
+    int st = 0;
     bool ok = true;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
       const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st & 1;
-      // one S/dP block: this step's S^T overwrites the block holding the previous dQ partial,
-      // so that partial is staged first (with two blocks it is staged after this step's P)
-      if (C::NBUF == 1 && st > 0 && !(ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh))) break;
       ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
       if (st >= 2) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - 2) / 2) & 1, abort_flag, p.status, 132);
@@ -418,60 +362,67 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
         const int c = half * C::CHUNKS_PER_WARP + cc;   // score chunk: queries [32c, 32c+32)
-        uint32_t sr[32], dr[32];
+        // the whole score chunk first (its upper half receives dS^T below), then dP^T / LSE / D
+        // 16 queries at a time
+        uint32_t sr[32];
         tmem_ld32(tb + c * 32, sr);
-        tmem_ld32(tb + BQ + c * 32, dr);
-        float l2[32], dv_[32];
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
-          const float4 a = ld_shared_f4(lse_s + (c * 32 + 4 * v4) * 4);
-          const float4 d = ld_shared_f4(lse_s + (BQ + c * 32 + 4 * v4) * 4);
-          l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
-          dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
-        }
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-        float pv[32];
-        if (full) {
+        for (int sub = 0; sub < 2; ++sub) {
+          const int q0 = c * 32 + sub * 16;   // first query of these 16
+          uint32_t dr[16];
+          tmem_ld16(tb + BQ + q0, dr);
+          float l2[16], dv_[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -l2[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = it.i0 + c * 32 + e;
-            bool vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
-            float bias = 0.f;
-            if (vis && code == TILE_MIXED) {
-              const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
-              if (s.mask_kind == MK_ADD) {
-                const float mv = static_cast<const float*>(p.mask)[midx];
-                vis = mv > kMaskFloor;
-                bias = mv * kLog2e;
-              } else {
-                vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
-              }
-            }
-            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, bias - l2[e])) : 0.f;
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const float4 a = ld_shared_f4(lse_s + (q0 + 4 * v4) * 4);
+            const float4 d = ld_shared_f4(lse_s + (BQ + q0 + 4 * v4) * 4);
+            l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
+            dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
           }
-        }
-        uint32_t pk[16], dk16[16];
+          tmem_wait_ld();
+          if (sub == 0) reg_fence(sr);
+          reg_fence16(dr);
+          float pv[16];
+          if (full) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          dk16[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
-                                pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
-        }
-        // P^T and dS^T of these 32 queries over this chunk's own (already read) score columns
-        tmem_st16(tb + c * 32, pk);
-        tmem_st16(tb + c * 32 + 16, dk16);
-        // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (4 x 16 B chunks per 32 queries)
+            for (int e = 0; e < 16; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
+          } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = c * 4 + u;              // 16-byte chunk among the BQ / 8 of this row
-          const int blk = chunk / 8, cin = chunk % 8;
-          st_shared_v4(sds + blk * C::DS_BLOCK + ((cin ^ (r & 7)) * 16), dk16[4 * u], dk16[4 * u + 1],
-                       dk16[4 * u + 2], dk16[4 * u + 3]);
+            for (int e = 0; e < 16; ++e) {
+              const int i = it.i0 + q0 + e;
+              bool vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
+              float bias = 0.f;
+              if (vis && code == TILE_MIXED) {
+                const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
+                if (s.mask_kind == MK_ADD) {
+                  const float mv = static_cast<const float*>(p.mask)[midx];
+                  vis = mv > kMaskFloor;
+                  bias = mv * kLog2e;
+                } else {
+                  vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
+                }
+              }
+              pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias - l2[e])) : 0.f;
+            }
+          }
+          uint32_t pk[8], dk8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+            dk8[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
+                                 pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
+          }
+          // P^T and dS^T of these 16 queries over this chunk's own (already read) score columns
+          tmem_st8(tb + c * 32 + sub * 8, pk);
+          tmem_st8(tb + c * 32 + 16 + sub * 8, dk8);
+          // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (2 x 16 B chunks)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int chunk = (q0 >> 3) + u;          // 16-byte chunk among the BQ / 8 of this row
+            const int blk = chunk / 8, cin = chunk % 8;
+            st_shared_v4(sds + blk * C::DS_BLOCK + ((cin ^ (r & 7)) * 16), dk8[4 * u], dk8[4 * u + 1],
+                         dk8[4 * u + 2], dk8[4 * u + 3]);
+          }
         }
       }
       tmem_wait_st();
@@ -482,14 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_arrive(&bar_p_full[buf]);
         mbar_arrive(&bar_lsed_empty[slot]);
       }
-      // the dQ partial of the previous step is ready by now (its MMA was issued before this step's P)
-      if (C::NBUF == 2 && st > 0 && !(ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh))) break;
-      prev_i0 = it.i0;
-      prev_hh = it.hh;
       ++st;
     }
-    if (ok && st > 0) ok = stage_dq(st - 1, st - 1, prev_i0, prev_hh);
-    if (leader) bulk_wait_group0();
     // ---- epilogue: dV and scale * dK of this thread's key, from TMEM; each warp of the
     //      quadrant pair takes half of the feature columns
     ok = __all_sync(0xffffffffu, ok);
@@ -540,6 +485,72 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
       }
     }
+  } else if (warp >= 12) {
+    // ---------------------------------------------------------------- dQ stager (warps 12-15)
+    // Each step's dQ partial: TMEM -> SMEM [BQ][D] fp32 -> dQ accumulator with one TMA
+    // reduce-add (the add happens in L2) issued by the leader thread.
+    const int wq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const bool leader = warp == 12 && lane == 0;
+    float* sdq = reinterpret_cast<float*>(smem + C::OFF_DQ);
+    const uint32_t sbase = smem_u32(sdq);
+    StepIter it;
+    it.init(G, s.Sq, BQ, ibeg);
+    int st = 0;
+    for (; it.valid(); it.next()) {
+      if (step_skipped(it)) continue;
+      const int buf = st % C::NBUF;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134)))
+        break;
+      if (st > 0) {
+        // the previous reduce-add must have finished reading the staging buffer
+        if (leader) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar_stage_free);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_stage_free, (st - 1) & 1, abort_flag, p.status, 135))) break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + hf * 32 + lane_off, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        if (C::DQ_TRANSPOSED) {
+          // thread = feature d, registers = queries 32*hf + e: row-major [q][d], lanes on consecutive d
+          const int d = wq * 32 + lane;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((hf * 32 + e) * D + d) * 4, __uint_as_float(v[e]));
+        } else {
+          // thread = query row, registers = features 32*hf + e; 16-byte chunks rotated across lanes
+          const int q = wq * 32 + lane;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cidx = (u + lane) & 7;
+            st_shared_v4(sbase + (q * D + hf * 32 + 4 * cidx) * 4, v[4 * cidx], v[4 * cidx + 1], v[4 * cidx + 2],
+                         v[4 * cidx + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_stage_full);
+      // the leader waits for all four warps' stores, then issues the reduce; its warp leaves
+      // the loop together if that wait gave up
+      bool filled = true;
+      if (leader) filled = mbar_wait(bar_stage_full, st & 1, abort_flag, p.status, 136);
+      if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
+      if (leader) {
+        tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, b * s.Hq + kvh * G + it.hh);
+        bulk_commit_group();
+      }
+      ++st;
+    }
+    if (leader) bulk_wait_group0();
   }
 
   tc_fence_before();
