@@ -57,7 +57,7 @@ struct BwdCfg {
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
   static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
-  static constexpr int NSTAGE = 2;                      // Q/dO ring depth
+  static constexpr int NSTAGE = D == 128 ? 3 : 2;       // Q/dO ring depth (fills shared memory)
   // shared memory (bytes)
   static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
   static constexpr int KV_TILE = kBN * D * 2;
@@ -74,6 +74,7 @@ struct BwdCfg {
   static constexpr int OFF_LSED = OFF_DQ + DQ_STAGE;               // [NSTAGE] x (lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
   static constexpr int BYTES = OFF_BAR + 512 + 1024;
+  static_assert(BYTES <= 232448, "shared memory per block");
 };
 
 struct BwdTcParams {
@@ -230,11 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       bool ok = mbar_wait(bar_kv, 0, abort_flag, p.status, 110);
       tc_fence_after();
 
-      auto first_half = [&](int st) -> bool {  // S^T, dP^T of step st
+      // S^T, dP^T of step st (its Q / dO are loaded and its S/dP TMEM block is free)
+      auto first_half = [&](int st) {
         const int slot = st % C::NSTAGE, buf = st % C::NBUF;
-        if (!mbar_wait(&bar_qdo_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 111)) return false;
-        if (st >= C::NBUF && !mbar_wait(&bar_dq_free[buf], ((st - C::NBUF) / C::NBUF) & 1, abort_flag, p.status, 112))
-          return false;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint32_t sdo = sq + C::Q_TILE;
@@ -253,11 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                  k > 0);
         }
         mma_commit(&bar_sdp_full[buf]);
-        return true;
       };
-      auto second_half = [&](int st) -> bool {  // dV, dK, dQ of step st
+      // dV, dK, dQ of step st (its P^T, dS^T are written)
+      auto second_half = [&](int st) {
         const int slot = st % C::NSTAGE, buf = st % C::NBUF, dsb = st & 1;
-        if (!mbar_wait(&bar_p_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 113)) return false;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint32_t sdo = sq + C::Q_TILE;
@@ -284,24 +282,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
         mma_commit(&bar_dq_full[buf]);
         mma_commit(&bar_ds_free[dsb]);
-        return true;
       };
 
-      StepIter it;
-      it.init(G, s.Sq, BQ, ibeg);
-      int n = 0;
-      for (; ok && it.valid(); it.next()) {
-        if (step_skipped(it)) continue;
-        if (C::NBUF == 1) {
-          if (n > 0 && !(ok = second_half(n - 1))) break;
-          if (!(ok = first_half(n))) break;
-        } else {
-          if (!(ok = first_half(n))) break;
-          if (n > 0 && !(ok = second_half(n - 1))) break;
-        }
-        ++n;
+      // Issue whichever half-step is ready: the second half of step ns (needs its P^T / dS^T) or
+      // the first half of step nf (needs its Q / dO and the dQ partial of step nf - NBUF drained
+      // from its TMEM block). A half-step that is waiting never holds back one that is ready.
+      int total = 0;
+      {
+        StepIter it;
+        it.init(G, s.Sq, BQ, ibeg);
+        for (; it.valid(); it.next())
+          if (!step_skipped(it)) ++total;
       }
-      if (ok && n > 0) ok = second_half(n - 1);
+      int nf = 0, ns = 0;
+      unsigned long long idle_since = globaltimer();
+      while (ok && ns < total) {
+        bool progressed = false;
+        if (ns < nf && mbar_test(&bar_p_full[ns % C::NBUF], (ns / C::NBUF) & 1)) {
+          second_half(ns++);
+          progressed = true;
+        } else if (nf < total && nf < ns + 2 &&
+                   mbar_test(&bar_qdo_full[nf % C::NSTAGE], (nf / C::NSTAGE) & 1) &&
+                   (nf < C::NBUF || mbar_test(&bar_dq_free[nf % C::NBUF], ((nf - C::NBUF) / C::NBUF) & 1))) {
+          first_half(nf++);
+          progressed = true;
+        }
+        if (progressed) {
+          idle_since = globaltimer();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if ((__nanosleep(20), globaltimer() - idle_since > kWaitLimitNs)) {
+          *abort_flag = 1;
+          atomicCAS(p.status, 0u, 0x80000000u | 111u);
+          ok = false;
+        }
+      }
       mma_commit(bar_mma_done);
       mbar_wait(bar_mma_done, 0, nullptr, p.status, 114);
     }
@@ -387,22 +402,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 16; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
           } else {
+            // visible query rows of this key are [rlo, rhi) (causal rule, query tail), relative to q0
+            const int base = it.i0 + q0;
+            int rlo = 0, rhi = key_ok && code != TILE_SKIP ? min(16, s.Sq - base) : 0;
+            if (s.causal) {
+              const long long first = (long long)j - s.q_offset - base;   // first row that sees key j
+              rlo = (int)max(0LL, min(first, 16LL));
+            }
+            if (code != TILE_MIXED) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int i = it.i0 + q0 + e;
-              bool vis = key_ok && i < s.Sq && (!s.causal || (long long)j <= s.q_offset + i) && code != TILE_SKIP;
-              float bias = 0.f;
-              if (vis && code == TILE_MIXED) {
-                const size_t midx = (mrow0 + i) * (size_t)s.Sk + j;
-                if (s.mask_kind == MK_ADD) {
-                  const float mv = static_cast<const float*>(p.mask)[midx];
-                  vis = mv > kMaskFloor;
-                  bias = mv * kLog2e;
-                } else {
-                  vis = static_cast<const uint8_t*>(p.mask)[midx] != 0;
-                }
+              for (int e = 0; e < 16; ++e)
+                pv[e] = (e >= rlo && e < rhi) ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e])) : 0.f;
+            } else {
+              // the 16 mask values of this key (one per query row) first, then the arithmetic
+              float bias[16];
+              if (s.mask_kind == MK_ADD) {
+                const float* mp = static_cast<const float*>(p.mask) + (mrow0 + base) * (size_t)s.Sk + j;
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  bias[e] = (e >= rlo && e < rhi) ? __ldg(mp + (size_t)e * s.Sk) : -CUDART_INF_F;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) bias[e] = bias[e] > kMaskFloor ? bias[e] * kLog2e : -CUDART_INF_F;
+              } else {
+                const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + (mrow0 + base) * (size_t)s.Sk + j;
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  bias[e] = (e >= rlo && e < rhi && __ldg(mp + (size_t)e * s.Sk) != 0) ? 0.f : -CUDART_INF_F;
               }
-              pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias - l2[e])) : 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                pv[e] = bias[e] != -CUDART_INF_F
+                            ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias[e] - l2[e]))
+                            : 0.f;
             }
           }
           uint32_t pk[8], dk8[8];
@@ -502,6 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const int buf = st % C::NBUF;
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134)))
         break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + lane_off, v[0]);
+      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + 32 + lane_off, v[1]);
+      tmem_wait_ld();
+      reg_fence(v[0]);
+      reg_fence(v[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);   // the TMEM block is free for step st + NBUF
       if (st > 0) {
         // the previous reduce-add must have finished reading the staging buffer
         if (leader) {
@@ -510,32 +551,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar_stage_free, (st - 1) & 1, abort_flag, p.status, 135))) break;
       }
-      tc_fence_after();
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t v[32];
-        tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + hf * 32 + lane_off, v);
-        tmem_wait_ld();
-        reg_fence(v);
         if (C::DQ_TRANSPOSED) {
           // thread = feature d, registers = queries 32*hf + e: row-major [q][d], lanes on consecutive d
           const int d = wq * 32 + lane;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((hf * 32 + e) * D + d) * 4, __uint_as_float(v[e]));
+          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((hf * 32 + e) * D + d) * 4, __uint_as_float(v[hf][e]));
         } else {
           // thread = query row, registers = features 32*hf + e; 16-byte chunks rotated across lanes
           const int q = wq * 32 + lane;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int cidx = (u + lane) & 7;
-            st_shared_v4(sbase + (q * D + hf * 32 + 4 * cidx) * 4, v[4 * cidx], v[4 * cidx + 1], v[4 * cidx + 2],
-                         v[4 * cidx + 3]);
+            st_shared_v4(sbase + (q * D + hf * 32 + 4 * cidx) * 4, v[hf][4 * cidx], v[hf][4 * cidx + 1],
+                         v[hf][4 * cidx + 2], v[hf][4 * cidx + 3]);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_stage_full);

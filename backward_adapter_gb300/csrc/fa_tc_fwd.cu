@@ -280,6 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const bool dead = (code == TILE_SKIP) || i >= s.Sq;
       const bool full = !dead && code == TILE_OPEN && key0 + kBN <= s.Sk && key0 + kBN - 1 <= causal_lim;
       // x_e = log2(e) * (scale * s_e + bias_e), or -inf where the pair is hidden
+      // last visible key of this row inside the tile (relative; -1 = none) from the causal rule
+      // and the key tail: one integer compare per element on partial tiles
+      int lim = 0;
+      if (!full && !dead) {
+        long long last = min((long long)s.Sk - 1, causal_lim) - key0;
+        lim = (int)max(-1LL, min(last, (long long)kBN - 1));
+      }
       auto masked = [&](uint32_t (&raw)[32], int c0, float (&x)[32]) {
         if (full) {
 #pragma unroll
@@ -287,23 +294,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         } else if (dead) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = -CUDART_INF_F;
-        } else {
+        } else if (code != TILE_MIXED) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int key = key0 + c0 + e;
-            bool vis = key < s.Sk && key <= causal_lim;
-            float bias = 0.f;
-            if (vis && code == TILE_MIXED) {
-              if (s.mask_kind == MK_ADD) {
-                const float mv = static_cast<const float*>(p.mask)[mrow + key];
-                vis = mv > kMaskFloor;
-                bias = mv * kLog2e;
-              } else {
-                vis = static_cast<const uint8_t*>(p.mask)[mrow + key] != 0;
-              }
-            }
-            x[e] = vis ? fmaf(__uint_as_float(raw[e]), sl2, bias) : -CUDART_INF_F;
-          }
+          for (int e = 0; e < 32; ++e) x[e] = (c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+        } else if (s.mask_kind == MK_ADD) {
+          // the row's 32 mask values first (independent loads), then the arithmetic
+          const float* mp = static_cast<const float*>(p.mask) + mrow + key0 + c0;
+          float mv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mv[e] = (c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            x[e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
+        } else {
+          const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + mrow + key0 + c0;
+          uint32_t mb8[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e <= lim) ? __ldg(mp + e) : 0u;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         }
       };
       // pass 1: row max of this tile
