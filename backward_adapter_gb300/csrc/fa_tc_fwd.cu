@@ -42,6 +42,9 @@ constexpr int kNumSms = 152;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr int kRegsControl = 80;
+constexpr int kRegsSoftmax = 208;
+static_assert((kRegsControl + 2 * kRegsSoftmax) * 128 <= kThreads * 168, "register split exceeds the launch pool");
 
 struct FwdTcParams {
   CUtensorMap tm_q, tm_k, tm_v;
@@ -154,8 +157,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
+  // Register split by warpgroup (setmaxnreg, inside each role's branch): the launch holds
+  // 384 x 168 registers; the control warpgroup keeps 80 and the two softmax warpgroups take 208
+  // each: (80 + 208 + 208) x 128 = 63488 <= 64512.
+  if (warp < 4) {
+   regs_dec<kRegsControl>();   // all four warps of the control warpgroup
+   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
@@ -195,9 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
-      const uint32_t tS[2] = {tmem + 0, tmem + 128};
-      const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
       const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      // one base descriptor per operand tile; every k-step adds a compile-time byte offset
+      auto issue_pv = [&](int t, int v_slot, uint32_t first_acc) {
+        const uint64_t dv0 = smem_desc_sw128(sKVa + v_slot * L::kTileBytes, L::kBoxBytes, 1024);
+        const uint32_t d_tmem = tmem + 256 + t * D, a_tmem = tmem + t * 128;
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)   // 16 keys (2048 B of V, 8 TMEM columns of P) per step
+          mma_ts(d_tmem, a_tmem + k * 8, desc_add(dv0, k * 2048), idesc_pv, (first_acc || k > 0) ? 1u : 0u);
+      };
+      auto issue_s = [&](int t, int k_slot) {
+        const uint64_t dq0 = smem_desc_sw128(sQa + t * L::kTileBytes, 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(sKVa + k_slot * L::kTileBytes, 16, 1024);
+        const uint32_t d_tmem = tmem + t * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * L::kBoxBytes + (k & 3) * 32;
+          mma_ss(d_tmem, desc_add(dq0, off), desc_add(dk0, off), idesc_qk, k > 0 ? 1u : 0u);
+        }
+      };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.status, 10);
       tc_fence_after();
       int idx = 0, c = 0;  // tiles processed, slots consumed
@@ -209,25 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const uint32_t k_phase = (c / L::kSlots) & 1;
         if (!(ok = mbar_wait(&bar_full[k_slot], k_phase, abort_flag, p.status, 11))) break;
         tc_fence_after();
+#pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
           if (idx > 0) {
             if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 12))) break;
             if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 13))) break;
             tc_fence_after();
-            const uint32_t vbase = sKVa + v_slot * L::kTileBytes;
-#pragma unroll
-            for (int k = 0; k < kBN / 16; ++k)
-              mma_ts(tO[t], tS[t] + k * 8, smem_desc_sw128(vbase + k * 16 * 128, L::kBoxBytes, 1024), idesc_pv,
-                     (idx - 1 > 0 || k > 0) ? 1u : 0u);
+            issue_pv(t, v_slot, idx - 1 > 0);
           }
-          const uint32_t qbase = sQa + t * L::kTileBytes;
-          const uint32_t kbase = sKVa + k_slot * L::kTileBytes;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * L::kBoxBytes + (k % 4) * 32;
-            mma_ss(tS[t], smem_desc_sw128(qbase + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024), idesc_qk,
-                   k > 0 ? 1u : 0u);
-          }
+          issue_s(t, k_slot);
           mma_commit(&bar_s[t]);
         }
         if (!ok) break;
@@ -239,15 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         ++idx;
       }
       if (ok && idx > 0) {
+#pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
           if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 14))) break;
           if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 15))) break;
           tc_fence_after();
-          const uint32_t vbase = sKVa + v_slot * L::kTileBytes;
-#pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            mma_ts(tO[t], tS[t] + k * 8, smem_desc_sw128(vbase + k * 16 * 128, L::kBoxBytes, 1024), idesc_pv,
-                   (idx - 1 > 0 || k > 0) ? 1u : 0u);
+          issue_pv(t, v_slot, idx - 1 > 0);
           mma_commit(&bar_o[t]);
         }
       }
@@ -255,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       mma_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr, p.status, 16);
     }
-  } else if (warp >= 4) {
+   }
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax, one row per thread
     const int t = (warp - 4) / 4;
     const int wq = warp & 3;                       // TMEM lane slice of this warp
@@ -287,16 +299,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         long long last = min((long long)s.Sk - 1, causal_lim) - key0;
         lim = (int)max(-1LL, min(last, (long long)kBN - 1));
       }
-      auto masked = [&](uint32_t (&raw)[32], int c0, float (&x)[32]) {
+      // the whole score row of this tile in registers (one TMEM wait), masked and scaled in place
+      float x[kBN];
+      auto masked = [&](const uint32_t (&raw)[32], int c0) {
         if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(raw[e]) * sl2;
+          for (int e = 0; e < 32; ++e) x[c0 + e] = __uint_as_float(raw[e]) * sl2;
         } else if (dead) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = -CUDART_INF_F;
+          for (int e = 0; e < 32; ++e) x[c0 + e] = -CUDART_INF_F;
         } else if (code != TILE_MIXED) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = (c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+          for (int e = 0; e < 32; ++e)
+            x[c0 + e] = (c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         } else if (s.mask_kind == MK_ADD) {
           // the row's 32 mask values first (independent loads), then the arithmetic
           const float* mp = static_cast<const float*>(p.mask) + mrow + key0 + c0;
@@ -305,52 +320,48 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           for (int e = 0; e < 32; ++e) mv[e] = (c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            x[e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
+            x[c0 + e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
         } else {
           const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + mrow + key0 + c0;
           uint32_t mb8[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e <= lim) ? __ldg(mp + e) : 0u;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+          for (int e = 0; e < 32; ++e) x[c0 + e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         }
       };
-      // pass 1: row max of this tile
       // (TMEM loads and stores are warp-collective: every lane issues them, hidden rows just get -inf)
+      {
+        uint32_t raw[2][32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tS + half * 64, raw[0]);
+          tmem_ld32(tS + half * 64 + 32, raw[1]);
+          tmem_wait_ld();
+          reg_fence(raw[0]);
+          reg_fence(raw[1]);
+          masked(raw[0], half * 64);
+          masked(raw[1], half * 64 + 32);
+        }
+      }
       float tm4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};  // 4 independent chains
 #pragma unroll
-      for (int cch = 0; cch < kBN / 32; ++cch) {
-        uint32_t raw[32];
-        float x[32];
-        tmem_ld32(tS + cch * 32, raw);
-        tmem_wait_ld();
-        reg_fence(raw);
-        masked(raw, cch * 32, x);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) tm4[e & 3] = fmaxf(tm4[e & 3], x[e]);
-      }
+      for (int e = 0; e < kBN; ++e) tm4[e & 3] = fmaxf(tm4[e & 3], x[e]);
       const float tmax = fmaxf(fmaxf(tm4[0], tm4[1]), fmaxf(tm4[2], tm4[3]));
       const float m_new = fmaxf(m, tmax);
       const bool rescale = m_new > m + kRescaleThreshold;   // false while nothing is visible
       const float m_use = rescale ? m_new : m;
       const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;
       const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-      // pass 2: P = 2^(x - m) as bf16 over the first 64 columns of the score block; chunk c of
-      // the scores is read before P chunk c lands on columns [16c, 16c + 16) (already read)
+      // P = 2^(x - m) as bf16 over the first 64 columns of the score block (all scores are in registers)
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cch = 0; cch < kBN / 32; ++cch) {
         uint32_t pk[16];
-        uint32_t raw[32];
-        float x[32];
-        tmem_ld32(tS + cch * 32, raw);
-        tmem_wait_ld();
-        reg_fence(raw);
-        masked(raw, cch * 32, x);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(x[2 * e] - m_sub);
-          const float p1 = ex2_approx(x[2 * e + 1] - m_sub);
+          const float p0 = ex2_approx(x[cch * 32 + 2 * e] - m_sub);
+          const float p1 = ex2_approx(x[cch * 32 + 2 * e + 1] - m_sub);
           sum4[e & 3] += p0 + p1;
           pk[e] = pack_bf16x2(p0, p1);
         }

@@ -292,6 +292,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Descriptor `d` advanced by `bytes` (a multiple of 16, staying inside the 256 KB shared window):
+// only the low 32-bit word changes, so no 64-bit arithmetic is needed.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = (uint32_t)d + (bytes >> 4), hi = (uint32_t)(d >> 32);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 // b_mn_major: B is stored with N contiguous (1) or K contiguous (0).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
