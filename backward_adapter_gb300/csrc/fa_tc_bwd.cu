@@ -231,26 +231,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       bool ok = mbar_wait(bar_kv, 0, abort_flag, p.status, 110);
       tc_fence_after();
 
+      // Base descriptors per operand tile; every k-step adds a compile-time byte offset (desc_add).
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dKmn = smem_desc_sw128(sK, C::KV_BOX, 1024);   // K as an MN-major operand
       // S^T, dP^T of step st (its Q / dO are loaded and its S/dP TMEM block is free)
       auto first_half = [&](int st) {
         const int slot = st % C::NSTAGE, buf = st % C::NBUF;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
-        const uint32_t sdo = sq + C::Q_TILE;
+        const uint64_t dq0 = smem_desc_sw128(sq, 16, 1024), ddo0 = smem_desc_sw128(sq + C::Q_TILE, 16, 1024);
         const uint32_t tb = tmem + buf * C::BUF_COLS;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k / 4) * C::KV_BOX + (k % 4) * 32;
-          const uint32_t qoff = (k / 4) * C::QBOX + (k % 4) * 32;
-          mma_ss(tb, smem_desc_sw128(sK + koff, 16, 1024), smem_desc_sw128(sq + qoff, 16, 1024), idesc_s, k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tb, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
+                 idesc_s, k > 0);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k / 4) * C::KV_BOX + (k % 4) * 32;
-          const uint32_t qoff = (k / 4) * C::QBOX + (k % 4) * 32;
-          mma_ss(tb + BQ, smem_desc_sw128(sV + koff, 16, 1024), smem_desc_sw128(sdo + qoff, 16, 1024), idesc_s,
-                 k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tb + BQ, desc_add(dV0, (k / 4) * C::KV_BOX + (k % 4) * 32),
+                 desc_add(ddo0, (k / 4) * C::QBOX + (k % 4) * 32), idesc_s, k > 0);
         mma_commit(&bar_sdp_full[buf]);
       };
       // dV, dK, dQ of step st (its P^T, dS^T are written)
@@ -258,27 +256,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int slot = st % C::NSTAGE, buf = st % C::NBUF, dsb = st & 1;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
-        const uint32_t sdo = sq + C::Q_TILE;
+        const uint64_t dqmn = smem_desc_sw128(sq, C::QBOX, 1024), ddomn = smem_desc_sw128(sq + C::Q_TILE, C::QBOX, 1024);
         const uint32_t tb = tmem + buf * C::BUF_COLS;
         // k-step k covers queries [16k, 16k+16): chunk k/2, columns (k%2)*8 within its P^T / dS^T half
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DV_COL, tb + 32 * (k / 2) + (k % 2) * 8, smem_desc_sw128(sdo + k * 2048, C::QBOX, 1024),
-                 idesc_g, (st > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, tb + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
+                 (st > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DK_COL, tb + 32 * (k / 2) + 16 + (k % 2) * 8,
-                 smem_desc_sw128(sq + k * 2048, C::QBOX, 1024), idesc_g, (st > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tb + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
+                 (st > 0 || k > 0) ? 1u : 0u);
         mma_commit(&bar_qdo_empty[slot]);
-        const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE);
+        const uint64_t ds0 = smem_desc_sw128(smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE), C::DS_BLOCK, 1024);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           if (C::DQ_TRANSPOSED)
-            mma_ss(tb + C::DQ_COL, smem_desc_sw128(sK + k * 2048, C::KV_BOX, 1024),
-                   smem_desc_sw128(sds + k * 2048, C::DS_BLOCK, 1024), idesc_q, k > 0);
+            mma_ss(tb + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
           else
-            mma_ss(tb + C::DQ_COL, smem_desc_sw128(sds + k * 2048, C::DS_BLOCK, 1024),
-                   smem_desc_sw128(sK + k * 2048, C::KV_BOX, 1024), idesc_q, k > 0);
+            mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
         }
         mma_commit(&bar_dq_full[buf]);
         mma_commit(&bar_ds_free[dsb]);
