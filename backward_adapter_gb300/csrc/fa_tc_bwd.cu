@@ -46,8 +46,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BQ = D == 128 ? 64 : 128;        // query rows per step
-  static constexpr int NBUF = D == 128 ? 2 : 1;         // S/dP TMEM blocks
+  static constexpr int BQ = 128;                        // query rows per step (every MMA has N = 128 or D)
+  static constexpr int NBUF = 1;                        // one S/dP TMEM block
   static constexpr int BUF_COLS = 2 * BQ;               // S^T [0,BQ), dP^T [BQ,2BQ)
   static constexpr int NCHUNK = BQ / 32;                // 32-column score chunks per step
   static constexpr int CHUNKS_PER_WARP = NCHUNK / 2;    // two warps per lane quadrant
@@ -57,7 +57,8 @@ struct BwdCfg {
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
   static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
-  static constexpr int NSTAGE = D == 128 ? 3 : 2;       // Q/dO ring depth (fills shared memory)
+  static constexpr int DQ_CHUNKS = (DQ_TRANSPOSED ? BQ : D) / 32;   // 32-column TMEM chunks of the dQ partial
+  static constexpr int NSTAGE = 2;                      // Q/dO ring depth
   // shared memory (bytes)
   static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
   static constexpr int KV_TILE = kBN * D * 2;
@@ -65,15 +66,16 @@ struct BwdCfg {
   static constexpr int Q_TILE = BQ * D * 2;
   static constexpr int DS_BLOCK = 128 * 128;            // 128 keys x 64 queries (bf16)
   static constexpr int DS_TILE = (BQ / 64) * DS_BLOCK;
-  static constexpr int DQ_STAGE = BQ * D * 4;           // fp32 [BQ][D] staging of the dQ partial
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
-  static constexpr int OFF_STAGE = 2 * KV_TILE;         // [NSTAGE] x (Q, dO)
-  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // [2] x dS^T
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;              // dQ staging
-  static constexpr int OFF_LSED = OFF_DQ + DQ_STAGE;               // [NSTAGE] x (lse2[BQ], dsum[BQ])
+  // [NSTAGE] x (Q, dO); once dV/dK of a step have read its slot, the slot holds that step's
+  // fp32 dQ partial ([BQ][D] = 2 * Q_TILE bytes) until the reduce-add has read it
+  static constexpr int OFF_STAGE = 2 * KV_TILE;
+  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // dS^T (the B / A operand of the dQ MMA)
+  static constexpr int OFF_LSED = OFF_DS + DS_TILE;                // [NSTAGE] x (lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
-  static constexpr int BYTES = OFF_BAR + 512 + 1024;
+  static constexpr int BYTES = OFF_BAR + 256;
+  static_assert(BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
   static_assert(BYTES <= 232448, "shared memory per block");
 };
 
@@ -116,8 +118,13 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  // the 128-byte swizzle of TMA and of the MMA descriptors assumes 1024-byte aligned tiles
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, 0x80000000u | 199u);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;                              // 1
   uint64_t* bar_qdo_full = bar_kv + 1;                  // NSTAGE
@@ -128,11 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_p_full = bar_sdp_full + C::NBUF;        // NBUF
   uint64_t* bar_dq_full = bar_p_full + C::NBUF;         // NBUF
   uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
-  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 2
-  uint64_t* bar_mma_done = bar_ds_free + 2;             // 1
-  uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 8 softmax-grad warps filled the dQ staging
-  uint64_t* bar_stage_free = bar_stage_full + 1;        // 1: the previous reduce finished reading it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_stage_free + 1);
+  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 1: the dQ MMA has read dS^T
+  uint64_t* bar_mma_done = bar_ds_free + 1;             // 1
+  uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 4 stager warps filled the dQ staging
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_stage_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* lsed = reinterpret_cast<float*>(smem + C::OFF_LSED);
 
@@ -166,11 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_dq_full[i], 1);
       mbar_init(&bar_dq_free[i], 4);
     }
-    mbar_init(&bar_ds_free[0], 1);
-    mbar_init(&bar_ds_free[1], 1);
+    mbar_init(bar_ds_free, 1);
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_stage_full, 4);
-    mbar_init(bar_stage_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -234,55 +238,60 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // Base descriptors per operand tile; every k-step adds a compile-time byte offset (desc_add).
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dKmn = smem_desc_sw128(sK, C::KV_BOX, 1024);   // K as an MN-major operand
-      // S^T, dP^T of step st (its Q / dO are loaded and its S/dP TMEM block is free)
-      auto first_half = [&](int st) {
-        const int slot = st % C::NSTAGE, buf = st % C::NBUF;
+      // S^T of step st: the score block's previous contents (P^T, dS^T of step st-1) were
+      // consumed by the dV / dK MMAs issued before (tcgen05 MMAs of a thread run in order)
+      auto issue_st = [&](int st) {
+        const int slot = st % C::NSTAGE;
         tc_fence_after();
-        const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
-        const uint64_t dq0 = smem_desc_sw128(sq, 16, 1024), ddo0 = smem_desc_sw128(sq + C::Q_TILE, 16, 1024);
-        const uint32_t tb = tmem + buf * C::BUF_COLS;
+        const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tb, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
+          mma_ss(tmem, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
                  idesc_s, k > 0);
+      };
+      // dP^T of step st: its TMEM block held the dQ partial of step st-1, drained by the stager
+      auto issue_dp = [&](int st) {
+        const int slot = st % C::NSTAGE;
+        tc_fence_after();
+        const uint64_t ddo0 =
+            smem_desc_sw128(smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE) + C::Q_TILE, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tb + BQ, desc_add(dV0, (k / 4) * C::KV_BOX + (k % 4) * 32),
+          mma_ss(tmem + BQ, desc_add(dV0, (k / 4) * C::KV_BOX + (k % 4) * 32),
                  desc_add(ddo0, (k / 4) * C::QBOX + (k % 4) * 32), idesc_s, k > 0);
-        mma_commit(&bar_sdp_full[buf]);
+        mma_commit(&bar_sdp_full[0]);
       };
       // dV, dK, dQ of step st (its P^T, dS^T are written)
       auto second_half = [&](int st) {
-        const int slot = st % C::NSTAGE, buf = st % C::NBUF, dsb = st & 1;
+        const int slot = st % C::NSTAGE;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint64_t dqmn = smem_desc_sw128(sq, C::QBOX, 1024), ddomn = smem_desc_sw128(sq + C::Q_TILE, C::QBOX, 1024);
-        const uint32_t tb = tmem + buf * C::BUF_COLS;
         // k-step k covers queries [16k, 16k+16): chunk k/2, columns (k%2)*8 within its P^T / dS^T half
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DV_COL, tb + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
+          mma_ts(tmem + C::DV_COL, tmem + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::DK_COL, tb + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
+          mma_ts(tmem + C::DK_COL, tmem + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar_qdo_empty[slot]);
-        const uint64_t ds0 = smem_desc_sw128(smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE), C::DS_BLOCK, 1024);
+        const uint64_t ds0 = smem_desc_sw128(smem_u32(smem + C::OFF_DS), C::DS_BLOCK, 1024);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           if (C::DQ_TRANSPOSED)
-            mma_ss(tb + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
+            mma_ss(tmem + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
           else
-            mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
+            mma_ss(tmem + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
         }
-        mma_commit(&bar_dq_full[buf]);
-        mma_commit(&bar_ds_free[dsb]);
+        mma_commit(&bar_dq_full[0]);
+        mma_commit(bar_ds_free);
       };
 
-      // Issue whichever half-step is ready: the second half of step ns (needs its P^T / dS^T) or
-      // the first half of step nf (needs its Q / dO and the dQ partial of step nf - NBUF drained
-      // from its TMEM block). A half-step that is waiting never holds back one that is ready.
+      // Issue whichever MMA group is ready; none that waits holds back one that is ready:
+      //   second half of step ns: after its P^T / dS^T are written;
+      //   dP^T of step np: after S^T(np) and once the stager drained the dQ partial of step np-1;
+      //   S^T of step nt: after its Q / dO are loaded and the second half of step nt-1 was issued.
       int total = 0;
       {
         StepIter it;
@@ -290,17 +299,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         for (; it.valid(); it.next())
           if (!step_skipped(it)) ++total;
       }
-      int nf = 0, ns = 0;
+      int nt = 0, np = 0, ns = 0;
       unsigned long long idle_since = globaltimer();
       while (ok && ns < total) {
         bool progressed = false;
-        if (ns < nf && mbar_test(&bar_p_full[ns % C::NBUF], (ns / C::NBUF) & 1)) {
+        if (ns < np && mbar_test(&bar_p_full[0], ns & 1)) {
           second_half(ns++);
           progressed = true;
-        } else if (nf < total && nf < ns + 2 &&
-                   mbar_test(&bar_qdo_full[nf % C::NSTAGE], (nf / C::NSTAGE) & 1) &&
-                   (nf < C::NBUF || mbar_test(&bar_dq_free[nf % C::NBUF], ((nf - C::NBUF) / C::NBUF) & 1))) {
-          first_half(nf++);
+        } else if (np < nt && (np == 0 || mbar_test(&bar_dq_free[0], (np - 1) & 1))) {
+          issue_dp(np++);
+          progressed = true;
+        } else if (nt < total && nt == ns && mbar_test(&bar_qdo_full[nt % C::NSTAGE], (nt / C::NSTAGE) & 1)) {
+          issue_st(nt++);
           progressed = true;
         }
         if (progressed) {
@@ -357,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     bool ok = true;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
-      const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st & 1;
-      ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
+      const int buf = 0, slot = st % C::NSTAGE;
+      ok = mbar_wait(&bar_sdp_full[0], st & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
-      if (st >= 2) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - 2) / 2) & 1, abort_flag, p.status, 132);
+      if (st >= 1) ok = ok && mbar_wait(bar_ds_free, (st - 1) & 1, abort_flag, p.status, 132);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // every pair of this step visible for this key: open tile, real rows, causal rule met by the first row
       const bool full = code == TILE_OPEN && key_ok && it.i0 + BQ <= s.Sq &&
                         (!s.causal || (long long)j <= s.q_offset + it.i0);
-      const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE) + r * 128;
+      const uint32_t sds = smem_u32(smem + C::OFF_DS) + r * 128;
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
         const int c = half * C::CHUNKS_PER_WARP + cc;   // score chunk: queries [32c, 32c+32)
@@ -519,63 +529,61 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
-    float* sdq = reinterpret_cast<float*>(smem + C::OFF_DQ);
-    const uint32_t sbase = smem_u32(sdq);
     StepIter it;
     it.init(G, s.Sq, BQ, ibeg);
     int st = 0;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
-      const int buf = st % C::NBUF;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134)))
-        break;
+      const int slot = st % C::NSTAGE;
+      float* sdq = reinterpret_cast<float*>(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
+      const uint32_t sbase = smem_u32(sdq);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[0], st & 1, abort_flag, p.status, 134))) break;
+      // the dQ partial (whose MMA ran after dV / dK had read this slot's Q and dO) into the slot
       tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + lane_off, v[0]);
-      tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + 32 + lane_off, v[1]);
-      tmem_wait_ld();
-      reg_fence(v[0]);
-      reg_fence(v[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);   // the TMEM block is free for step st + NBUF
-      if (st > 0) {
-        // the previous reduce-add must have finished reading the staging buffer
-        if (leader) {
-          bulk_wait_group_read0();
-          mbar_arrive(bar_stage_free);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_stage_free, (st - 1) & 1, abort_flag, p.status, 135))) break;
-      }
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        if (C::DQ_TRANSPOSED) {
-          // thread = feature d, registers = queries 32*hf + e: row-major [q][d], lanes on consecutive d
-          const int d = wq * 32 + lane;
+      for (int c2 = 0; c2 < C::DQ_CHUNKS; c2 += 2) {
+        uint32_t v[2][32];
+        tmem_ld32(tmem + C::DQ_COL + c2 * 32 + lane_off, v[0]);
+        tmem_ld32(tmem + C::DQ_COL + (c2 + 1) * 32 + lane_off, v[1]);
+        tmem_wait_ld();
+        reg_fence(v[0]);
+        reg_fence(v[1]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((hf * 32 + e) * D + d) * 4, __uint_as_float(v[hf][e]));
-        } else {
-          // thread = query row, registers = features 32*hf + e; 16-byte chunks rotated across lanes
-          const int q = wq * 32 + lane;
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c = c2 + hf;
+          if (C::DQ_TRANSPOSED) {
+            // thread = feature d, registers = queries 32c + e: row-major [q][d], lanes on consecutive d
+            const int d = wq * 32 + lane;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int cidx = (u + lane) & 7;
-            st_shared_v4(sbase + (q * D + hf * 32 + 4 * cidx) * 4, v[hf][4 * cidx], v[hf][4 * cidx + 1],
-                         v[hf][4 * cidx + 2], v[hf][4 * cidx + 3]);
+            for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((c * 32 + e) * D + d) * 4, __uint_as_float(v[hf][e]));
+          } else {
+            // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
+            const int q = wq * 32 + lane;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int cidx = (u + lane) & 7;
+              st_shared_v4(sbase + (q * D + c * 32 + 4 * cidx) * 4, v[hf][4 * cidx], v[hf][4 * cidx + 1],
+                           v[hf][4 * cidx + 2], v[hf][4 * cidx + 3]);
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dq_free[0]);   // the TMEM block is free for the next dP^T
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_stage_full);
-      // the leader waits for all four warps' stores, then issues the reduce; its warp leaves
-      // the loop together if that wait gave up
+      // the leader waits for all four warps' stores, issues the reduce, and hands the slot back to
+      // the producer once the reduce has read it; its warp leaves the loop together on a timeout
       bool filled = true;
       if (leader) filled = mbar_wait(bar_stage_full, st & 1, abort_flag, p.status, 136);
       if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
       if (leader) {
         tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, b * s.Hq + kvh * G + it.hh);
         bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&bar_qdo_empty[slot]);
       }
       ++st;
     }
