@@ -135,6 +135,8 @@ cudaError_t prof_end(int kid, cudaStream_t st) {
 }
 void count_launches(int n) { g_launches += (uint64_t)n; }
 
+void set_error_message(const char* msg) { set_error("%s", msg); }
+
 unsigned* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

@@ -68,6 +68,9 @@ struct BwdPlan {
   size_t total;
 };
 
+// Sets the calling thread's fa_last_error() text.
+void set_error_message(const char* msg);
+
 // Device status word the kernels' bounded waits report into (nullptr if unavailable).
 unsigned* device_status_ptr();
 

@@ -23,7 +23,7 @@ FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
-            "fa_profile_launch_count", "fa_device_status")
+            "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_profile_set_events.restype = st
     lib.fa_profile_launch_count.argtypes = []
     lib.fa_profile_launch_count.restype = ctypes.c_uint64
+    lib.fa_train_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.fa_train_bwd_noalloc.restype = st
     lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_device_status.restype = st
     _lib = lib
@@ -229,3 +231,27 @@ def device_status() -> int:
     v = ctypes.c_uint32(0)
     _check(load_library().fa_device_status(ctypes.byref(v)))
     return int(v.value)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, dq=None, dk=None,
+                dv=None, stream=None):
+    """Backward through fa_train_bwd_noalloc: no workspace is allocated or passed.
+
+    For callers that cannot allocate device memory (their memory is owned by another
+    allocator, or allocation is not allowed where they run). The library keeps the scratch in
+    a fixed 16 MiB device array; larger shapes raise FaError (FA_ERR_WORKSPACE). Calls that
+    overlap on the GPU share that array and race.
+    """
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, k, v, o, lse, do, mview)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib.fa_train_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                    _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(q.device, stream)))
+    return dq, dk, dv

@@ -157,6 +157,25 @@ FA_API fa_status fa_profile_set_events(int kernel, void* start_event, void* stop
 FA_API uint64_t fa_profile_launch_count(void);
 
 /*
+ * Allocation-free backward (no counterpart in the pages; an addition for callers of this
+ * library that cannot allocate device memory: a framework pool or plugin host that owns all of
+ * the GPU's memory and hands over only its tensors, or a loop where a cudaMalloc and the
+ * device synchronisation it can imply are not allowed). Same arguments, results and errors as
+ * fa_train_bwd without ws / ws_bytes: the scratch lives in one static device array of
+ * 16 MiB (16777216 bytes) inside the library, which every GPU that loads the library holds
+ * until the process exits. Shapes whose fa_train_bwd_workspace_size() exceeds 16 MiB are
+ * rejected with FA_ERR_WORKSPACE (and a message in fa_last_error()) before anything runs.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, once
+ * per device, with that device current); make that first call before any stream capture.
+ * The library allocates and frees nothing in this call. Every call shares the one array and
+ * the kernels re-initialise what must start at zero, so back-to-back calls on one stream are
+ * fine, but calls that overlap on the GPU (other streams, other host threads) race.
+ */
+FA_API fa_status fa_train_bwd_noalloc(const fa_params* p, const void* q, const void* k, const void* v,
+                                      const void* mask, const void* o, const float* lse, const void* dO,
+                                      void* dq, void* dk, void* dv, void* stream);
+
+/*
  * Reads and clears the status word of the current device's kernels: 0 when
  * every wait inside a kernel completed; otherwise 0x80000000 | site, where site
  * names the wait that ran out of its time limit (the kernel then stopped early
