@@ -41,7 +41,13 @@ namespace {
 using namespace tc;
 
 constexpr int kBN = 128;       // keys per CTA
-constexpr int kThreads = 512;  // 16 warps = 4 warpgroups (128 registers per thread)
+constexpr int kThreads = 512;  // 16 warps = 4 warpgroups (128 registers per thread at launch)
+// Register split by warpgroup (setmaxnreg, inside each role's branch): control warps 0-3 keep 80,
+// the softmax-grad warpgroups keep 128, the dQ stager (warps 12-15) takes 176 so it can hold a
+// whole dQ partial row: (80 + 128 + 128 + 176) x 128 = 65536 = 512 x 128.
+constexpr int kRegsControl = 80;
+constexpr int kRegsStager = 176;
+static_assert(kRegsControl + 2 * 128 + kRegsStager <= 4 * 128, "register split exceeds the launch pool");
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -133,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_lsed_empty = bar_lsed_full + C::NSTAGE; // NSTAGE
   uint64_t* bar_sdp_full = bar_lsed_empty + C::NSTAGE;  // NBUF
   uint64_t* bar_p_full = bar_sdp_full + C::NBUF;        // NBUF
-  uint64_t* bar_dq_full = bar_p_full + C::NBUF;         // NBUF
+  uint64_t* bar_p_half = bar_p_full + C::NBUF;          // 1: P^T / dS^T of the step's first 64 queries
+  uint64_t* bar_dq_full = bar_p_half + 1;               // NBUF
   uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
   uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 1: the dQ MMA has read dS^T
   uint64_t* bar_mma_done = bar_ds_free + 1;             // 1
@@ -173,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_dq_free[i], 4);
     }
     mbar_init(bar_ds_free, 1);
+    mbar_init(bar_p_half, 8);
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_stage_full, 4);
     *abort_flag = 0;
@@ -186,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 
   auto step_skipped = [&](const StepIter& it) { return bwd_tile_code(p, mb, it.i0, kt) == TILE_SKIP; };
 
-  if (warp == 0) {
+  if (warp < 4) {
+   regs_dec<kRegsControl>();   // all four warps of the control warpgroup
+   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
@@ -261,21 +271,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                  desc_add(ddo0, (k / 4) * C::QBOX + (k % 4) * 32), idesc_s, k > 0);
         mma_commit(&bar_sdp_full[0]);
       };
-      // dV, dK, dQ of step st (its P^T, dS^T are written)
-      auto second_half = [&](int st) {
+      // dV, dK over the step's queries [64h, 64h + 64): k-step k covers queries [16k, 16k+16),
+      // score chunk k/2, columns (k%2)*8 within its P^T / dS^T half
+      auto issue_dvdk = [&](int st, int h) {
         const int slot = st % C::NSTAGE;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint64_t dqmn = smem_desc_sw128(sq, C::QBOX, 1024), ddomn = smem_desc_sw128(sq + C::Q_TILE, C::QBOX, 1024);
-        // k-step k covers queries [16k, 16k+16): chunk k/2, columns (k%2)*8 within its P^T / dS^T half
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
+        for (int kk = 0; kk < BQ / 32; ++kk) {
+          const int k = h * (BQ / 32) + kk;
           mma_ts(tmem + C::DV_COL, tmem + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
+        }
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
+        for (int kk = 0; kk < BQ / 32; ++kk) {
+          const int k = h * (BQ / 32) + kk;
           mma_ts(tmem + C::DK_COL, tmem + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
+        }
+      };
+      // dQ of step st (all of its dS^T is in shared memory)
+      auto issue_dq = [&](int st) {
         const uint64_t ds0 = smem_desc_sw128(smem_u32(smem + C::OFF_DS), C::DS_BLOCK, 1024);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
@@ -289,9 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       };
 
       // Issue whichever MMA group is ready; none that waits holds back one that is ready:
-      //   second half of step ns: after its P^T / dS^T are written;
+      //   dV/dK of step ns, first 64 queries: once their P^T / dS^T are written;
+      //   dV/dK of the other 64 queries and dQ of step ns: once all of its P^T / dS^T are written;
       //   dP^T of step np: after S^T(np) and once the stager drained the dQ partial of step np-1;
-      //   S^T of step nt: after its Q / dO are loaded and the second half of step nt-1 was issued.
+      //   S^T of step nt: after its Q / dO are loaded and step nt-1 was issued completely.
+      // The issue order of the groups that accumulate (dV, dK) is fixed, so they are bitwise
+      // reproducible.
       int total = 0;
       {
         StepIter it;
@@ -299,12 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         for (; it.valid(); it.next())
           if (!step_skipped(it)) ++total;
       }
-      int nt = 0, np = 0, ns = 0;
+      int nt = 0, np = 0, ns = 0, na = 0;   // na: steps whose first-half dV/dK are issued
       unsigned long long idle_since = globaltimer();
       while (ok && ns < total) {
         bool progressed = false;
-        if (ns < np && mbar_test(&bar_p_full[0], ns & 1)) {
-          second_half(ns++);
+        if (na == ns && ns < np && mbar_test(bar_p_half, ns & 1)) {
+          issue_dvdk(ns, 0);
+          ++na;
+          progressed = true;
+        } else if (na > ns && mbar_test(&bar_p_full[0], ns & 1)) {
+          issue_dvdk(ns, 1);
+          issue_dq(ns++);
           progressed = true;
         } else if (np < nt && (np == 0 || mbar_test(&bar_dq_free[0], (np - 1) & 1))) {
           issue_dp(np++);
@@ -350,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&bar_lsed_full[slot]);
       ++st;
     }
-  } else if (warp >= 4 && warp < 12) {
+   }
+  } else if (warp < 12) {
     // ---------------------------------------------------------------- softmax-grad
     const int wq = warp & 3;                      // TMEM lane quadrant
     const int half = (warp - 4) >> 2;             // which half of the step's query columns
@@ -382,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const uint32_t sds = smem_u32(smem + C::OFF_DS) + r * 128;
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
-        const int c = half * C::CHUNKS_PER_WARP + cc;   // score chunk: queries [32c, 32c+32)
+        // round cc covers queries [64cc, 64cc + 64): the two warps of a lane quadrant take one
+        // 32-query chunk each, and the first round is handed to the dV / dK MMAs right away
+        const int c = cc * 2 + half;   // score chunk: queries [32c, 32c+32)
         // the whole score chunk first (its upper half receives dS^T below), then dP^T / LSE / D
         // 16 queries at a time
         uint32_t sr[32];
@@ -461,6 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                          dk8[4 * u + 2], dk8[4 * u + 3]);
           }
         }
+        if (cc == 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_p_half);
+        }
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -522,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
       }
     }
-  } else if (warp >= 12) {
+  } else {
+    regs_inc<kRegsStager>();
     // ---------------------------------------------------------------- dQ stager (warps 12-15)
     // Each step's dQ partial: TMEM -> SMEM [BQ][D] fp32 -> dQ accumulator with one TMA
     // reduce-add (the add happens in L2) issued by the leader thread.
@@ -538,39 +573,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       float* sdq = reinterpret_cast<float*>(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
       const uint32_t sbase = smem_u32(sdq);
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[0], st & 1, abort_flag, p.status, 134))) break;
-      // the dQ partial (whose MMA ran after dV / dK had read this slot's Q and dO) into the slot
+      // the whole dQ partial row of this thread into registers, so the TMEM block is released at once
       tc_fence_after();
+      uint32_t v[C::DQ_CHUNKS][32];
 #pragma unroll
-      for (int c2 = 0; c2 < C::DQ_CHUNKS; c2 += 2) {
-        uint32_t v[2][32];
-        tmem_ld32(tmem + C::DQ_COL + c2 * 32 + lane_off, v[0]);
-        tmem_ld32(tmem + C::DQ_COL + (c2 + 1) * 32 + lane_off, v[1]);
-        tmem_wait_ld();
-        reg_fence(v[0]);
-        reg_fence(v[1]);
+      for (int c = 0; c < C::DQ_CHUNKS; ++c) tmem_ld32(tmem + C::DQ_COL + c * 32 + lane_off, v[c]);
+      tmem_wait_ld();
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int c = c2 + hf;
-          if (C::DQ_TRANSPOSED) {
-            // thread = feature d, registers = queries 32c + e: row-major [q][d], lanes on consecutive d
-            const int d = wq * 32 + lane;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((c * 32 + e) * D + d) * 4, __uint_as_float(v[hf][e]));
-          } else {
-            // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
-            const int q = wq * 32 + lane;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int cidx = (u + lane) & 7;
-              st_shared_v4(sbase + (q * D + c * 32 + 4 * cidx) * 4, v[hf][4 * cidx], v[hf][4 * cidx + 1],
-                           v[hf][4 * cidx + 2], v[hf][4 * cidx + 3]);
-            }
-          }
-        }
-      }
+      for (int c = 0; c < C::DQ_CHUNKS; ++c) reg_fence(v[c]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_dq_free[0]);   // the TMEM block is free for the next dP^T
+      // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read
+#pragma unroll
+      for (int c = 0; c < C::DQ_CHUNKS; ++c) {
+        if (C::DQ_TRANSPOSED) {
+          // thread = feature d, registers = queries 32c + e: row-major [q][d], lanes on consecutive d
+          const int d = wq * 32 + lane;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((c * 32 + e) * D + d) * 4, __uint_as_float(v[c][e]));
+        } else {
+          // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
+          const int q = wq * 32 + lane;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cidx = (u + lane) & 7;
+            st_shared_v4(sbase + (q * D + c * 32 + 4 * cidx) * 4, v[c][4 * cidx], v[c][4 * cidx + 1],
+                         v[c][4 * cidx + 2], v[c][4 * cidx + 3]);
+          }
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_stage_full);
