@@ -275,6 +275,15 @@ fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const void* k, c
   return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream);
 }
 
+fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream) {
+  if (limit_ms == 0 || limit_ms > 10000) {
+    set_error("limit_ms=%u outside [1, 10000]", limit_ms);
+    return FA_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_wait_selftest((unsigned long long)limit_ms * 1000000ull, (cudaStream_t)stream),
+                     "wait self-test launch");
+}
+
 const char* fa_status_str(fa_status s) {
   switch (s) {
     case FA_OK: return "ok";

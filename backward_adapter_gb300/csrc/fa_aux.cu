@@ -6,12 +6,14 @@
 //   * mask tile classification: one byte per 128x128 tile saying whether the
 //     tile is fully hidden (skipped), fully open with zero bias (no mask reads
 //     in the hot loop) or mixed.
-// Each thread moves 16-byte vectors; rows are split across 8..16 lanes.
+// Each thread moves 16-byte vectors; rows are split across 8..16 lanes. The file also holds
+// the self-test of the kernels' bounded waits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
+#include "tc_ptx.cuh"
 
 namespace fa {
 namespace {
@@ -168,6 +170,36 @@ cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tile
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_MASK, st);
+}
+
+}  // namespace fa
+
+// ---------------------------------------------------------------------------------------------
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing ever arrives on,
+// with a short limit; the wait gives up, records its site in the status word and the kernel
+// returns normally, leaving the context usable.
+// ---------------------------------------------------------------------------------------------
+
+namespace fa {
+namespace {
+
+__global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  tc::mbar_init(&bar, 1);
+  tc::fence_barrier_init();
+  __syncwarp();
+  // phase 0 never completes: nobody arrives
+  tc::mbar_wait(&bar, 0, nullptr, status, kSelfTestSite, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorUnknown;
+  wait_selftest_kernel<<<1, 1, 0, st>>>(status, limit_ns);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

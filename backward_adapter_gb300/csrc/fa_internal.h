@@ -74,6 +74,10 @@ void set_error_message(const char* msg);
 // Device status word the kernels' bounded waits report into (nullptr if unavailable).
 unsigned* device_status_ptr();
 
+// Self-test of the kernels' bounded waits (see fa_train_selftest_wait).
+constexpr unsigned kSelfTestSite = 900;
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
+
 // Tracing hooks (fa_profile_set_events): per-thread events recorded around a
 // kernel family, and a per-thread launch counter.
 enum : int { KID_FWD = 0, KID_BWD_MAIN = 1, KID_BWD_DSUM = 2, KID_BWD_DQCONV = 3, KID_MASK = 4, KID_COUNT = 5 };

@@ -75,14 +75,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // records `site` in the error word and in *abort) if it does not complete
 // within the time limit, or if another role of the block has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status,
-                                          unsigned site) {
+                                          unsigned site, unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
         atomicCAS(status, 0u, 0x80000000u | site);
         return false;
@@ -128,11 +128,6 @@ __device__ __forceinline__ void regs_dec() {
 template <int N>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-// Named barrier over `count` threads (a multiple of 32) of the block.
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t saddr, float v) {

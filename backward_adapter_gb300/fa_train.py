@@ -23,7 +23,7 @@ FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
-            "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc")
+            "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc", "fa_train_selftest_wait")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_profile_launch_count.restype = ctypes.c_uint64
     lib.fa_train_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.fa_train_bwd_noalloc.restype = st
+    lib.fa_train_selftest_wait.argtypes = [ctypes.c_uint32, vp]
+    lib.fa_train_selftest_wait.restype = st
     lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_device_status.restype = st
     _lib = lib
@@ -224,6 +226,16 @@ def profile_set_events(kernel: int, start=None, stop=None) -> None:
 def profile_launch_count() -> int:
     """Kernels the library has launched from this thread so far."""
     return int(load_library().fa_profile_launch_count())
+
+
+WAIT_SELFTEST_SITE = 900
+
+
+def selftest_wait(limit_ms: int = 50, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nothing ever satisfies); see device_status()."""
+    import torch as _torch
+    dev = _torch.device("cuda", _torch.cuda.current_device())
+    _check(load_library().fa_train_selftest_wait(int(limit_ms), _stream(dev, stream)))
 
 
 def device_status() -> int:

@@ -184,6 +184,14 @@ FA_API fa_status fa_train_bwd_noalloc(const fa_params* p, const void* q, const v
  */
 FA_API fa_status fa_device_status(uint32_t* out);
 
+/*
+ * Self-test of the failure detection: launches one thread that waits on an mbarrier nothing ever
+ * arrives on, with the given limit (1..10000 ms). The wait gives up, writes 0x80000000 | 900 into
+ * the status word that fa_device_status() reads, and the kernel returns normally (the CUDA
+ * context stays usable). Asynchronous on `stream` like the op calls.
+ */
+FA_API fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream);
+
 /* Static description of a status code. */
 FA_API const char* fa_status_str(fa_status s);
 
