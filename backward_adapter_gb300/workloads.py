@@ -42,6 +42,7 @@ class Workload:
     dtype: str = "bf16"          # "f32" or "bf16": input/output element type
     causal: bool = False
     q_offset: int = 0            # query row i sits at key position q_offset + i
+    window: int = 0              # sliding window half-width (0 = none)
     mask: str = "none"           # none | extra_row | pad_self | cross | random_bool | random_add
     accum: bool = False          # dK/dV accumulate into prefilled fp32 buffers
     do_std: float = 1.0          # standard deviation of dO
@@ -185,6 +186,8 @@ def visible_pairs(w: Workload) -> int:
             vis &= (mb != 0) if kind == "bool" else (mb > -1e9)
         if w.causal:
             vis &= j <= w.q_offset + i
+        if w.window > 0:
+            vis &= np.abs(w.q_offset + i - j) <= w.window
         total += int(vis.sum())
     return total * w.Hq
 

@@ -35,7 +35,11 @@ Readings where the pages are silent (each listed in the design notes):
   * LSE is a natural logarithm;
   * GQA maps query head h to key/value head floor(h / G), G = Hq / Hkv
     (consecutive query heads share one key/value head);
-  * causal: key j is visible to query i iff j <= q_offset + i.
+  * causal: key j is visible to query i iff j <= q_offset + i;
+  * sliding window w > 0 (the DiT self-attention mask of HOT-Step TRAINING.md, "DiT
+    micro-batching": a sliding window plus padded key columns): key j is visible to query i
+    only if |q_offset + i - j| <= w; with causal only the left side applies
+    (q_offset + i - w <= j <= q_offset + i).
 
 Arrays are numpy, [B, H, S, D] row-major; masks are [Bm, Sq, Sk] with Bm in
 {1, B}. All arithmetic is float64 on the exact input values.
@@ -47,7 +51,7 @@ import numpy as np
 MASK_FLOOR = -1e9
 
 
-def visibility(Sq: int, Sk: int, mask_b, mask_kind: str, causal: bool, q_offset: int) -> np.ndarray:
+def visibility(Sq: int, Sk: int, mask_b, mask_kind: str, causal: bool, q_offset: int, window: int = 0) -> np.ndarray:
     """Boolean [Sq, Sk]: True where query i may attend to key j."""
     vis = np.ones((Sq, Sk), dtype=bool)
     if mask_b is not None and mask_kind != "none":
@@ -57,10 +61,12 @@ def visibility(Sq: int, Sk: int, mask_b, mask_kind: str, causal: bool, q_offset:
             vis &= np.asarray(mask_b, dtype=np.float64) > MASK_FLOOR
         else:
             raise ValueError(mask_kind)
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
     if causal:
-        i = np.arange(Sq)[:, None]
-        j = np.arange(Sk)[None, :]
         vis &= j <= q_offset + i
+    if window > 0:
+        vis &= np.abs(q_offset + i - j) <= window
     return vis
 
 
@@ -76,10 +82,10 @@ def _mask_for_batch(mask, b):
     return mask[b if mask.shape[0] > 1 else 0]
 
 
-def head_probabilities(q_h, k_h, scale, mask_b, mask_kind, causal, q_offset):
+def head_probabilities(q_h, k_h, scale, mask_b, mask_kind, causal, q_offset, window=0):
     """P [Sq, Sk], LSE [Sq] and the row-has-a-visible-key flag for one head."""
     Sq, Sk = q_h.shape[0], k_h.shape[0]
-    vis = visibility(Sq, Sk, mask_b, mask_kind, causal, q_offset)
+    vis = visibility(Sq, Sk, mask_b, mask_kind, causal, q_offset, window)
     s = scale * (q_h @ k_h.T) + _bias(mask_b, mask_kind, vis)
     s = np.where(vis, s, -np.inf)
     alive = vis.any(axis=1)
@@ -96,7 +102,7 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def forward(q, k, v, scale, mask=None, mask_kind="none", causal=False, q_offset=0):
+def forward(q, k, v, scale, mask=None, mask_kind="none", causal=False, q_offset=0, window=0):
     """Return O [B,Hq,Sq,D] and LSE [B,Hq,Sq], both float64."""
     q, k, v = _as64(q), _as64(k), _as64(v)
     B, Hq, Sq, D = q.shape
@@ -108,12 +114,12 @@ def forward(q, k, v, scale, mask=None, mask_kind="none", causal=False, q_offset=
         mb = _mask_for_batch(mask, b)
         for h in range(Hq):
             kv = h // G
-            p, lse[b, h], _ = head_probabilities(q[b, h], k[b, kv], scale, mb, mask_kind, causal, q_offset)
+            p, lse[b, h], _ = head_probabilities(q[b, h], k[b, kv], scale, mb, mask_kind, causal, q_offset, window)
             o[b, h] = p @ v[b, kv]
     return o, lse
 
 
-def backward(q, k, v, do, scale, mask=None, mask_kind="none", causal=False, q_offset=0):
+def backward(q, k, v, do, scale, mask=None, mask_kind="none", causal=False, q_offset=0, window=0):
     """Return dict with o, lse, d (= rowsum(dO*O)), dq, dk, dv (float64).
 
     P is rebuilt from its definition, not from a stored LSE, so the backward
@@ -133,7 +139,7 @@ def backward(q, k, v, do, scale, mask=None, mask_kind="none", causal=False, q_of
         mb = _mask_for_batch(mask, b)
         for h in range(Hq):
             kv = h // G
-            p, lse[b, h], _ = head_probabilities(q[b, h], k[b, kv], scale, mb, mask_kind, causal, q_offset)
+            p, lse[b, h], _ = head_probabilities(q[b, h], k[b, kv], scale, mb, mask_kind, causal, q_offset, window)
             o[b, h] = p @ v[b, kv]
             dsum[b, h] = (do[b, h] * o[b, h]).sum(axis=1)
             dp = do[b, h] @ v[b, kv].T
@@ -144,7 +150,7 @@ def backward(q, k, v, do, scale, mask=None, mask_kind="none", causal=False, q_of
     return {"o": o, "lse": lse, "d": dsum, "dq": dq, "dk": dk, "dv": dv}
 
 
-def probabilities(q, k, scale, mask=None, mask_kind="none", causal=False, q_offset=0):
+def probabilities(q, k, scale, mask=None, mask_kind="none", causal=False, q_offset=0, window=0):
     """P [B,Hq,Sq,Sk] (float64): exposed so tests can check its invariants."""
     q, k = _as64(q), _as64(k)
     B, Hq, Sq, _ = q.shape
@@ -154,18 +160,19 @@ def probabilities(q, k, scale, mask=None, mask_kind="none", causal=False, q_offs
     for b in range(B):
         mb = _mask_for_batch(mask, b)
         for h in range(Hq):
-            out[b, h], _, _ = head_probabilities(q[b, h], k[b, h // G], scale, mb, mask_kind, causal, q_offset)
+            out[b, h], _, _ = head_probabilities(q[b, h], k[b, h // G], scale, mb, mask_kind, causal, q_offset,
+                                                 window)
     return out
 
 
 def backward_accumulate(q, k, v, do, dk_acc, dv_acc, scale, mask=None, mask_kind="none", causal=False,
-                        q_offset=0):
+                        q_offset=0, window=0):
     """Accumulating backward: dK/dV are added to caller-owned buffers.
 
     llama.cpp PR #57, commit 86c140d (ggml_opt_accumulate_grad): the backward
     adds a node's gradient into an existing tensor. Sums are taken in float64.
     """
-    r = backward(q, k, v, do, scale, mask, mask_kind, causal, q_offset)
+    r = backward(q, k, v, do, scale, mask, mask_kind, causal, q_offset, window)
     r["dk"] = _as64(dk_acc) + r["dk"]
     r["dv"] = _as64(dv_acc) + r["dv"]
     return r

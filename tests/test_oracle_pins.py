@@ -27,7 +27,7 @@ def _tiny(seed=0, B=1, Hq=2, Hkv=1, Sq=5, Sk=7, D=4):
 
 
 def _variants():
-    """(name, mask, kind, causal, q_offset) over a 5x7 score matrix."""
+    """(name, mask, kind, causal, q_offset, window) over a 5x7 score matrix."""
     rng = np.random.default_rng(42)
     bias = rng.standard_normal((1, 5, 7)) * 0.7
     bias_masked = bias.copy()
@@ -36,28 +36,30 @@ def _variants():
     boolm = (rng.random((1, 5, 7)) < 0.6).astype(np.uint8)
     boolm[0, :, 0] = 1                          # keep every row alive
     return [
-        ("plain", None, "none", False, 0),
-        ("causal_offset", None, "none", True, 2),
-        ("additive_bias", bias_masked, "add", False, 0),
-        ("bool", boolm, "bool", False, 0),
-        ("causal_and_bias", bias, "add", True, 3),
+        ("plain", None, "none", False, 0, 0),
+        ("causal_offset", None, "none", True, 2, 0),
+        ("additive_bias", bias_masked, "add", False, 0, 0),
+        ("bool", boolm, "bool", False, 0, 0),
+        ("causal_and_bias", bias, "add", True, 3, 0),
+        ("window_sym", None, "none", False, 1, 2),
+        ("window_causal_bias", bias, "add", True, 2, 1),
     ]
 
 
 VARIANTS = _variants()
 
 
-@pytest.mark.parametrize("name,mask,kind,causal,off", VARIANTS, ids=[v[0] for v in VARIANTS])
-def test_softmax_rows_sum_to_one(name, mask, kind, causal, off):
+@pytest.mark.parametrize("name,mask,kind,causal,off,win", VARIANTS, ids=[v[0] for v in VARIANTS])
+def test_softmax_rows_sum_to_one(name, mask, kind, causal, off, win):
     q, k, v, _ = _tiny(1)
-    p = ref.probabilities(q, k, 0.5, mask, kind, causal, off)
+    p = ref.probabilities(q, k, 0.5, mask, kind, causal, off, win)
     np.testing.assert_allclose(p.sum(-1), 1.0, atol=1e-12)
-    vis = ref.visibility(5, 7, None if mask is None else mask[0], kind, causal, off)
+    vis = ref.visibility(5, 7, None if mask is None else mask[0], kind, causal, off, win)
     assert np.all(p[..., ~vis] == 0.0)
 
 
-@pytest.mark.parametrize("name,mask,kind,causal,off", VARIANTS, ids=[v[0] for v in VARIANTS])
-def test_gradients_match_central_differences(name, mask, kind, causal, off):
+@pytest.mark.parametrize("name,mask,kind,causal,off,win", VARIANTS, ids=[v[0] for v in VARIANTS])
+def test_gradients_match_central_differences(name, mask, kind, causal, off, win):
     """Central differences of L = sum(G * O) with a seeded non-zero G.
 
     The skill page's trap list (item 7) warns that a zero loss gradient
@@ -66,10 +68,10 @@ def test_gradients_match_central_differences(name, mask, kind, causal, off):
     """
     q, k, v, g = _tiny(2)
     scale = 0.6
-    r = ref.backward(q, k, v, g, scale, mask, kind, causal, off)
+    r = ref.backward(q, k, v, g, scale, mask, kind, causal, off, win)
 
     def loss(q_, k_, v_):
-        o, _ = ref.forward(q_, k_, v_, scale, mask, kind, causal, off)
+        o, _ = ref.forward(q_, k_, v_, scale, mask, kind, causal, off, win)
         return float((g * o).sum())
 
     h = 1e-6
@@ -86,7 +88,7 @@ def test_gradients_match_central_differences(name, mask, kind, causal, off):
         np.testing.assert_allclose(an, fd, rtol=1e-6, atol=1e-6 * np.abs(an).max())
 
 
-def _sdpa_fp64(q, k, v, g, scale, mask, kind, causal, off):
+def _sdpa_fp64(q, k, v, g, scale, mask, kind, causal, off, win=0):
     """PyTorch's scaled_dot_product_attention (float64, CPU) with autograd."""
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
@@ -104,20 +106,22 @@ def _sdpa_fp64(q, k, v, g, scale, mask, kind, causal, off):
         else:
             attn = attn + torch.where(m <= -1e9, torch.tensor(-math.inf, dtype=torch.float64),
                                       m.double())[:, None]
+    i = torch.arange(Sq)[:, None]
+    j = torch.arange(Sk)[None, :]
     if causal:
-        i = torch.arange(Sq)[:, None]
-        j = torch.arange(Sk)[None, :]
         attn = attn.masked_fill(~(j <= off + i), -math.inf)
+    if win > 0:
+        attn = attn.masked_fill((off + i - j).abs() > win, -math.inf)
     o = torch.nn.functional.scaled_dot_product_attention(tq, ke, ve, attn_mask=attn, scale=scale)
     o.backward(torch.tensor(g))
     return o.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
 
 
-@pytest.mark.parametrize("name,mask,kind,causal,off", VARIANTS, ids=[v[0] for v in VARIANTS])
-def test_matches_torch_sdpa_float64(name, mask, kind, causal, off):
+@pytest.mark.parametrize("name,mask,kind,causal,off,win", VARIANTS, ids=[v[0] for v in VARIANTS])
+def test_matches_torch_sdpa_float64(name, mask, kind, causal, off, win):
     q, k, v, g = _tiny(3, B=1, Hq=4, Hkv=2, Sq=5, Sk=7, D=8)
-    r = ref.backward(q, k, v, g, 0.35, mask, kind, causal, off)
-    o, dq, dk, dv = _sdpa_fp64(q, k, v, g, 0.35, mask, kind, causal, off)
+    r = ref.backward(q, k, v, g, 0.35, mask, kind, causal, off, win)
+    o, dq, dk, dv = _sdpa_fp64(q, k, v, g, 0.35, mask, kind, causal, off, win)
     for a, b in ((r["o"], o), (r["dq"], dq), (r["dk"], dk), (r["dv"], dv)):
         np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
 
@@ -205,13 +209,13 @@ def test_single_key_closed_form():
     np.testing.assert_allclose(r["dv"][0, 0, 0], g[0].sum(axis=(0, 1)), atol=1e-13)
 
 
-@pytest.mark.parametrize("name,mask,kind,causal,off", VARIANTS, ids=[v[0] for v in VARIANTS])
-def test_dk_sums_to_zero_and_d_is_p_dot_dp(name, mask, kind, causal, off):
+@pytest.mark.parametrize("name,mask,kind,causal,off,win", VARIANTS, ids=[v[0] for v in VARIANTS])
+def test_dk_sums_to_zero_and_d_is_p_dot_dp(name, mask, kind, causal, off, win):
     """sum_j dS_ij = 0 (hence sum_j dK_j = 0), and D_i = sum_j P_ij dP_ij."""
     q, k, v, g = _tiny(9)
-    r = ref.backward(q, k, v, g, 0.5, mask, kind, causal, off)
+    r = ref.backward(q, k, v, g, 0.5, mask, kind, causal, off, win)
     np.testing.assert_allclose(r["dk"].sum(axis=2), 0.0, atol=1e-13)
-    p = ref.probabilities(q, k, 0.5, mask, kind, causal, off)
+    p = ref.probabilities(q, k, 0.5, mask, kind, causal, off, win)
     dp = np.einsum("bhid,bjd->bhij", g, v[:, 0])
     np.testing.assert_allclose((p * dp).sum(-1), r["d"], atol=1e-13)
 
@@ -310,3 +314,41 @@ def test_mask_recipes_have_the_stated_structure():
         assert int(np.all(m[b] == -np.inf, axis=1).sum()) == 2
     m, _ = wl.make_mask(wl.TINY_F32)
     assert np.all(m[0, 64] == -np.inf) and np.all(m[0, :64] == 0)
+
+
+def test_window_equals_the_same_band_as_an_explicit_mask():
+    """The sliding window gives exactly what an additive mask hiding the same pairs gives."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 1, 9, 13, 8
+    q, k, v, g = (_rand(rng, B, Hq, Sq, D), _rand(rng, B, Hkv, Sk, D), _rand(rng, B, Hkv, Sk, D),
+                  _rand(rng, B, Hq, Sq, D))
+    for causal, off, win in ((False, 2, 3), (True, 4, 2), (False, 0, 1)):
+        i = np.arange(Sq)[:, None]
+        j = np.arange(Sk)[None, :]
+        band = np.abs(off + i - j) <= win
+        mask = np.where(band, 0.0, -np.inf)[None]
+        a = ref.backward(q, k, v, g, 0.4, causal=causal, q_offset=off, window=win)
+        b = ref.backward(q, k, v, g, 0.4, mask, "add", causal=causal, q_offset=off)
+        for key in ("o", "lse", "dq", "dk", "dv"):
+            np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_window_wider_than_the_sequence_changes_nothing():
+    q, k, v, g = _tiny(18)
+    a = ref.backward(q, k, v, g, 0.5, causal=True, q_offset=2)
+    b = ref.backward(q, k, v, g, 0.5, causal=True, q_offset=2, window=100)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_window_zero_width_band_is_the_diagonal():
+    """Window 1 around the diagonal with Sq = Sk: closed form for Q = 0 (mean of <= 3 values)."""
+    rng = np.random.default_rng(19)
+    S, D = 6, 4
+    q = np.zeros((1, 1, S, D))
+    k, v = _rand(rng, 1, 1, S, D), _rand(rng, 1, 1, S, D)
+    o, lse = ref.forward(q, k, v, 0.5, window=1)
+    for i in range(S):
+        vis = [j for j in range(S) if abs(i - j) <= 1]
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, vis].mean(0), atol=1e-14)
+        np.testing.assert_allclose(lse[0, 0, i], math.log(len(vis)), atol=1e-14)
