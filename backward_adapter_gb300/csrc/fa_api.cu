@@ -50,16 +50,20 @@ fa_status check_params(const fa_params* p, Shape& s) {
   if (p->mask_kind != FA_MASK_NONE && p->mask_batch != 1 && p->mask_batch != p->B) {
     set_error("mask_batch=%d must be 1 or B=%d", p->mask_batch, p->B); return FA_ERR_INVALID_ARG;
   }
-  if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
-  if (p->causal && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
-    set_error("causal q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
+  if (p->window < 0) { set_error("window=%d must be >= 0 (0 = no window)", p->window); return FA_ERR_INVALID_ARG; }
+  const bool positioned = p->causal || p->window > 0;
+  if (positioned && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
+    set_error("q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
               (long long)p->q_offset, p->Sq, p->Sk);
     return FA_ERR_INVALID_ARG;
   }
   s.B = p->B; s.Hq = p->Hq; s.Hkv = p->Hkv; s.Sq = p->Sq; s.Sk = p->Sk; s.D = p->D;
   s.dtype = p->dtype; s.scale = p->scale; s.causal = p->causal; s.mask_kind = p->mask_kind;
   s.mask_batch = p->mask_kind == FA_MASK_NONE ? 1 : p->mask_batch;
-  s.q_offset = p->causal ? (long long)p->q_offset : 0;
+  // with q_offset + Sq <= Sk no pair is further apart than Sk - 1, so a window of Sk or more hides
+  // nothing: drop it so no kernel pays for it
+  s.window = (p->window > 0 && p->window < p->Sk) ? p->window : 0;
+  s.q_offset = (p->causal || s.window > 0) ? (long long)p->q_offset : 0;
   return FA_OK;
 }
 

@@ -39,6 +39,7 @@ __device__ __forceinline__ bool pair_visible(const Shape& s, const void* mask, i
   bias = 0.f;
   if (i >= s.Sq || j >= s.Sk) return false;
   if (s.causal && (long long)j > s.q_offset + i) return false;
+  if (s.window > 0 && llabs(s.q_offset + i - (long long)j) > s.window) return false;
   if (s.mask_kind != MK_NONE) {
     const size_t mb = (s.mask_batch > 1) ? (size_t)b : 0;
     const size_t idx = (mb * (size_t)s.Sq + (size_t)i) * (size_t)s.Sk + (size_t)j;

@@ -20,7 +20,8 @@ struct Shape {
   int causal;
   int mask_kind;
   int mask_batch;
-  long long q_offset;
+  int window;          // sliding-window half-width, 0 = none
+  long long q_offset;  // key position of query row 0 (0 unless causal or windowed)
 };
 
 struct FwdArgs {

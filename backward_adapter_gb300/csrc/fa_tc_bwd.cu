@@ -100,18 +100,19 @@ struct BwdTcParams {
   unsigned* status;
 };
 
-// The steps of a CTA: (query head of the group, query tile) pairs in a fixed order.
+// The steps of a CTA: (query head of the group, query tile) pairs in a fixed order; the tiles
+// run over the rows [ibeg, iend) that can see the CTA's keys.
 struct StepIter {
-  int G, Sq, BQ, ibeg;
+  int G, iend, BQ, ibeg;
   int hh, i0;
-  __device__ void init(int G_, int Sq_, int BQ_, int ibeg_) {
-    G = G_; Sq = Sq_; BQ = BQ_; ibeg = ibeg_;
+  __device__ void init(int G_, int iend_, int BQ_, int ibeg_) {
+    G = G_; iend = iend_; BQ = BQ_; ibeg = ibeg_;
     hh = 0; i0 = ibeg;
   }
-  __device__ bool valid() const { return hh < G && ibeg < Sq; }
+  __device__ bool valid() const { return hh < G && ibeg < iend; }
   __device__ void next() {
     i0 += BQ;
-    if (i0 >= Sq) { i0 = ibeg; ++hh; }
+    if (i0 >= iend) { i0 = ibeg; ++hh; }
   }
 };
 
@@ -159,11 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
   const int j0 = kt * kBN;
   const int mb = s.mask_batch > 1 ? b : 0;
-  int ibeg = 0;
-  if (s.causal) {
-    const long long first = (long long)j0 - s.q_offset;  // rows below this see none of the keys
-    ibeg = first <= 0 ? 0 : (int)((first / BQ) * BQ);
+  // query rows that can see a key of this tile: [first, last] from the causal rule and the window
+  long long first = 0, last = (long long)s.Sq - 1;
+  if (s.causal) first = (long long)j0 - s.q_offset;
+  if (s.window > 0) {
+    if (!s.causal) first = (long long)j0 - s.q_offset - s.window;
+    last = min(last, (long long)j0 + kBN - 1 - s.q_offset + s.window);
   }
+  const int ibeg = first <= 0 ? 0 : (int)min((first / BQ) * BQ, (long long)s.Sq);
+  const int iend = (int)max((long long)ibeg, last + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       }
       uint32_t used_mask = 0, phase_mask = 0;
       StepIter it;
-      it.init(G, s.Sq, BQ, ibeg);
+      it.init(G, iend, BQ, ibeg);
       for (int st = 0; it.valid(); it.next()) {
         if (step_skipped(it)) continue;
         const int slot = st % C::NSTAGE;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       int total = 0;
       {
         StepIter it;
-        it.init(G, s.Sq, BQ, ibeg);
+        it.init(G, iend, BQ, ibeg);
         for (; it.valid(); it.next())
           if (!step_skipped(it)) ++total;
       }
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else if (warp == 2) {
     // ---------------------------------------------------------------- LSE / D staging
     StepIter it;
-    it.init(G, s.Sq, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg);
     const float l2e = kLog2e;
     for (int st = 0; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
@@ -386,9 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const float sl2 = s.scale * kLog2e;
     const bool key_ok = j < s.Sk;
     const size_t mrow0 = (size_t)mb * s.Sq;
+    // query rows that see this key: [row_lo, row_hi] from the causal rule and the window
+    long long row_lo = 0, row_hi = (long long)s.Sq - 1;
+    if (s.causal) row_lo = (long long)j - s.q_offset;
+    if (s.window > 0) {
+      if (!s.causal) row_lo = (long long)j - s.q_offset - s.window;
+      row_hi = min(row_hi, (long long)j - s.q_offset + s.window);
+    }
 
     StepIter it;
-    it.init(G, s.Sq, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg);
     int st = 0;
     bool ok = true;
     for (; it.valid(); it.next()) {
@@ -402,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
       const uint32_t lse_s = smem_u32(lsed + slot * 2 * BQ);  // [lse * log2(e) x BQ | D x BQ]
       const int code = bwd_tile_code(p, mb, it.i0, kt);
-      // every pair of this step visible for this key: open tile, real rows, causal rule met by the first row
-      const bool full = code == TILE_OPEN && key_ok && it.i0 + BQ <= s.Sq &&
-                        (!s.causal || (long long)j <= s.q_offset + it.i0);
+      // every pair of this step visible for this key: open tile, real key, all BQ rows inside the
+      // key's row band (which also ends at the last real row)
+      const bool full = code == TILE_OPEN && key_ok && it.i0 >= row_lo && (long long)it.i0 + BQ - 1 <= row_hi;
       const uint32_t sds = smem_u32(smem + C::OFF_DS) + r * 128;
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
@@ -436,13 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 16; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
           } else {
-            // visible query rows of this key are [rlo, rhi) (causal rule, query tail), relative to q0
+            // visible query rows of this key are [rlo, rhi) relative to base (causal rule, window,
+            // query tail); rhi <= rlo when none is
             const int base = it.i0 + q0;
-            int rlo = 0, rhi = key_ok && code != TILE_SKIP ? min(16, s.Sq - base) : 0;
-            if (s.causal) {
-              const long long first = (long long)j - s.q_offset - base;   // first row that sees key j
-              rlo = (int)max(0LL, min(first, 16LL));
-            }
+            const int rlo = (int)max(0LL, min(row_lo - base, 16LL));
+            const int rhi = key_ok && code != TILE_SKIP ? (int)max(0LL, min(row_hi - base + 1, 16LL)) : 0;
             if (code != TILE_MIXED) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
     StepIter it;
-    it.init(G, s.Sq, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg);
     int st = 0;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;

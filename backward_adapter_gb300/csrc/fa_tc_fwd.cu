@@ -72,23 +72,26 @@ struct FwdSmem {
   static constexpr int kBytes = kBarOff + 256 + 1024;    // barriers + alignment slack
 };
 
-// Key-tile range of a CTA after causal clipping and the split.
+// Key-tile range of a CTA after causal / sliding-window clipping and the split.
 struct KvRange {
   int begin, end;  // tile indices [begin, end)
 };
 
 __device__ __forceinline__ KvRange kv_range(const FwdTcParams& p, int q_row0, int split) {
   const Shape& s = p.s;
-  long long kv_end = s.Sk;
-  if (s.causal) {
-    const long long last_row = (long long)min(q_row0 + kRowsPerCta, s.Sq) - 1;
-    kv_end = min(kv_end, s.q_offset + last_row + 1);
+  const long long last_row = (long long)min(q_row0 + kRowsPerCta, s.Sq) - 1;
+  long long kv_beg = 0, kv_end = s.Sk;
+  if (s.causal) kv_end = min(kv_end, s.q_offset + last_row + 1);
+  if (s.window > 0) {
+    kv_beg = max(0LL, s.q_offset + q_row0 - s.window);
+    kv_end = min(kv_end, s.q_offset + last_row + s.window + 1);
   }
-  const int n = (int)((kv_end + kBN - 1) / kBN);
+  const int t0 = (int)(kv_beg / kBN);
+  const int n = max(0, (int)((kv_end + kBN - 1) / kBN) - t0);
   const int per = (n + p.kv_splits - 1) / p.kv_splits;
   KvRange r;
-  r.begin = min(n, split * per);
-  r.end = min(n, r.begin + per);
+  r.begin = t0 + min(n, split * per);
+  r.end = t0 + min(n, split * per + per);
   return r;
 }
 
@@ -277,7 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * D + lane_off;
     const float sl2 = s.scale * kLog2e;
-    const long long causal_lim = s.causal ? s.q_offset + i : (long long)INT32_MAX;
+    // visible keys of this row: [key_lo, key_hi] from the causal rule and the window
+    long long key_lo = 0, key_hi = (long long)s.Sk - 1;
+    if (s.causal) key_hi = min(key_hi, s.q_offset + i);
+    if (s.window > 0) {
+      key_lo = s.q_offset + i - s.window;
+      key_hi = min(key_hi, s.q_offset + i + s.window);
+    }
     const size_t mrow = ((size_t)mb * s.Sq + (size_t)min(i, s.Sq - 1)) * (size_t)s.Sk;
     float m = -CUDART_INF_F, l = 0.f;
     int idx = 0;
@@ -290,14 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const int code = tile_code(p, mb, qt0 + t, j);
       const int key0 = j * kBN;
       const bool dead = (code == TILE_SKIP) || i >= s.Sq;
-      const bool full = !dead && code == TILE_OPEN && key0 + kBN <= s.Sk && key0 + kBN - 1 <= causal_lim;
+      const bool full = !dead && code == TILE_OPEN && key0 >= key_lo && key0 + kBN - 1 <= key_hi;
       // x_e = log2(e) * (scale * s_e + bias_e), or -inf where the pair is hidden
-      // last visible key of this row inside the tile (relative; -1 = none) from the causal rule
-      // and the key tail: one integer compare per element on partial tiles
-      int lim = 0;
+      // first / last visible key of this row inside the tile (relative; lim < lo = none) from the
+      // causal rule, the window and the key tail: integer compares per element on partial tiles
+      int lo = 0, lim = 0;
       if (!full && !dead) {
-        long long last = min((long long)s.Sk - 1, causal_lim) - key0;
-        lim = (int)max(-1LL, min(last, (long long)kBN - 1));
+        lo = (int)max(0LL, min(key_lo - key0, (long long)kBN));
+        lim = (int)max(-1LL, min(key_hi - key0, (long long)kBN - 1));
       }
       // the whole score row of this tile in registers (one TMEM wait), masked and scaled in place
       float x[kBN];
@@ -311,13 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         } else if (code != TILE_MIXED) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            x[c0 + e] = (c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+            x[c0 + e] = (c0 + e >= lo && c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         } else if (s.mask_kind == MK_ADD) {
           // the row's 32 mask values first (independent loads), then the arithmetic
           const float* mp = static_cast<const float*>(p.mask) + mrow + key0 + c0;
           float mv[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mv[e] = (c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
+          for (int e = 0; e < 32; ++e) mv[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             x[c0 + e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + mrow + key0 + c0;
           uint32_t mb8[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e <= lim) ? __ldg(mp + e) : 0u;
+          for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : 0u;
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c0 + e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         }
@@ -507,7 +516,10 @@ int n_qpairs(const Shape& s) { return (s.Sq + kRowsPerCta - 1) / kRowsPerCta; }
 int kv_tiles_total(const Shape& s) {
   long long kv_end = s.Sk;
   if (s.causal) kv_end = min(kv_end, s.q_offset + s.Sq);
-  return (int)((kv_end + kBN - 1) / kBN);
+  int n = (int)((kv_end + kBN - 1) / kBN);
+  // a window confines a CTA's rows to a band of 2w + kRowsPerCta keys
+  if (s.window > 0) n = (int)min((long long)n, (2LL * s.window + kRowsPerCta + kBN - 1) / kBN + 1);
+  return n;
 }
 
 }  // namespace

@@ -10,7 +10,8 @@ values (the oracle widens the rounded values to float64).
 Workload shapes follow the pages' use of the op:
   * DiT self-attention with padded key columns and GQA (HOT-Step TRAINING.md,
     "DiT micro-batching": padded KV columns are masked for valid query rows,
-    padded query rows keep the pad columns open);
+    padded query rows keep the pad columns open), with or without the sliding
+    window of the other self-attention layer type;
   * DiT cross-attention with a per-batch encoder length (flash-attn-training
     skill, trap list item 8: the cross mask is the one that masks whole key
     columns; item 9: fully-masked query rows);
@@ -70,7 +71,13 @@ LONG_WINDOW = Workload("chunk512_window67584_h16_kv4_d128_accum", B=1, Hq=16, Hk
                        Sk=67584, D=128, causal=True, q_offset=67072, accum=True, seed=1005)
 
 WORKLOADS = [TINY_F32, DIT_SELF, DIT_CROSS, CAUSAL_LM, LONG_WINDOW]
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# The other DiT self-attention mask: a sliding window plus the padded key columns (the pages give
+# no width; 128 keys on either side is the reading used here).
+DIT_SELF_WINDOW = Workload("dit_self_window128_gqa_pad_s1024_d64", B=1, Hq=16, Hkv=8, Sq=1024, Sk=1024, D=64,
+                           window=128, mask="pad_self", seed=1006)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [DIT_SELF_WINDOW]}
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:

@@ -185,7 +185,7 @@ def oracle_sample(w: wl.Workload, inputs: dict, n_heads: int):
     if mask is not None:
         mask = mask[:1]
     t0 = time.perf_counter()
-    ref.backward(q, k, v, do, w.scale, mask, inputs["mask_kind"], w.causal, w.q_offset)
+    ref.backward(q, k, v, do, w.scale, mask, inputs["mask_kind"], w.causal, w.q_offset, w.window)
     dt = time.perf_counter() - t0
     pairs_per_head = wl.visible_pairs(w.with_(B=1, Hq=1, Hkv=1))
     fl = 14.0 * w.D * pairs_per_head * n_heads
@@ -253,7 +253,7 @@ def run_ours(args):
         host["mask"] = torch.from_numpy(inputs["mask"]).pin_memory()
     d = {n: t.to(dev) for n, t in host.items()}
     mask = d.get("mask")
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window)
     p = ft.make_params(d["q"], d["k"], mask, **kw)
     ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
@@ -420,7 +420,7 @@ def run_ours(args):
         "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
-                   "causal": w.causal, "q_offset": w.q_offset, "mask": w.mask, "accum": w.accum,
+                   "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask, "accum": w.accum,
                    "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
                    "l2": "flushed (256 MiB write) between timed steps, outside the step events",
                    "parallelism": f"replicas x{world}"},

@@ -24,8 +24,14 @@
  *     (its probability is exactly 0); any larger value is a bias added after scaling.
  *   - Boolean mask (FA_MASK_BOOL_U8): 1 = attend, 0 = hidden.
  *   - Causal: key j is visible to query i iff j <= q_offset + i (a query chunk
- *     sitting at positions q_offset.. of a longer cached window). Mask and
- *     causal combine (a pair must pass both).
+ *     sitting at positions q_offset.. of a longer cached window).
+ *   - Sliding window w > 0 (HOT-Step TRAINING.md, "DiT micro-batching": the DiT
+ *     self-attention mask is a sliding window plus padded key columns; the page
+ *     gives no width convention, so w is the half-width): key j is visible to
+ *     query i iff |q_offset + i - j| <= w. With causal only the left half remains
+ *     (q_offset + i - w <= j <= q_offset + i). The band is analytic: no mask
+ *     tensor is read for it, and key tiles outside it are never loaded.
+ *   - Mask, causal rule and window combine: a pair must pass all that are set.
  *   - LSE is a natural logarithm. O, dQ, dK, dV have the input element type;
  *     bf16 results are rounded to nearest even from fp32 accumulators.
  *
@@ -89,8 +95,9 @@ typedef struct fa_params {
   int32_t causal;     /* 0 or 1 */
   int32_t mask_kind;  /* fa_mask_kind */
   int32_t mask_batch; /* 1 (broadcast over batch) or B; ignored without a mask */
-  int32_t reserved;   /* must be 0 */
-  int64_t q_offset;   /* causal only: key position of query row 0; needs 0 <= q_offset and q_offset + Sq <= Sk */
+  int32_t window;     /* sliding-window half-width w >= 0; 0 = no window */
+  int64_t q_offset;   /* causal or window > 0: key position of query row 0; needs 0 <= q_offset and
+                         q_offset + Sq <= Sk. Ignored (taken as 0) when neither is set. */
 } fa_params;
 
 /* Bytes of scratch the forward needs for these parameters (0 when none). */

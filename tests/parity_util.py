@@ -31,7 +31,7 @@ def to_device(inputs: dict, w: wl.Workload, device="cuda"):
 
 def run_gpu(w: wl.Workload, t: dict) -> dict:
     """Forward + backward on the GPU; returns float64 numpy copies of every output."""
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window)
     o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
     if w.accum:
         dk, dv = t["dk_acc"].clone(), t["dv_acc"].clone()
@@ -51,7 +51,8 @@ def run_oracle(w: wl.Workload, inputs: dict, q_heads=None, kv_heads=None) -> dic
         q, do = q[:, q_heads], do[:, q_heads]
         k, v = k[:, kv_heads], v[:, kv_heads]
     args = (q, k, v, do)
-    kw = dict(mask=inputs["mask"], mask_kind=inputs["mask_kind"], causal=w.causal, q_offset=w.q_offset)
+    kw = dict(mask=inputs["mask"], mask_kind=inputs["mask_kind"], causal=w.causal, q_offset=w.q_offset,
+              window=w.window)
     if w.accum:
         dka, dva = inputs["dk_acc"], inputs["dv_acc"]
         if kv_heads is not None:
@@ -83,20 +84,17 @@ def assert_parity(w: wl.Workload, got: dict, exp: dict, where: str = ""):
 
 
 def assert_exact_zeros(w: wl.Workload, inputs: dict, got: dict, q_heads=None):
-    """Fully-masked query rows: O = 0, LSE = 0, dQ = 0 exactly. Hidden key columns: dK = dV = 0 exactly."""
+    """Query rows that see no key: O = 0, LSE = 0, dQ = 0 exactly. Keys no query sees (mask,
+    causal rule or window): dK = dV = 0 exactly (the accumulator unchanged under accumulation)."""
     mask, kind = inputs["mask"], inputs["mask_kind"]
-    if mask is None:
-        return
-    hidden = (mask == 0) if kind == "bool" else ~(mask > -1e9)
-    dead_rows = hidden.all(axis=2)    # [Bm, Sq]
-    dead_cols = hidden.all(axis=1)    # [Bm, Sk]
     for b in range(w.B):
-        mb = b if mask.shape[0] > 1 else 0
-        rows = np.nonzero(dead_rows[mb])[0]
+        mb = None if mask is None else mask[b if mask.shape[0] > 1 else 0]
+        vis = ref.visibility(w.Sq, w.Sk, mb, kind, w.causal, w.q_offset, w.window)
+        rows = np.nonzero(~vis.any(axis=1))[0]
         if rows.size:
             assert np.all(got["o"][b][:, rows] == 0) and np.all(got["lse"][b][:, rows] == 0)
             assert np.all(got["dq"][b][:, rows] == 0)
-        cols = np.nonzero(dead_cols[mb])[0]
+        cols = np.nonzero(~vis.any(axis=0))[0]
         if cols.size and not w.accum:
             assert np.all(got["dk"][b][:, cols] == 0) and np.all(got["dv"][b][:, cols] == 0)
         if cols.size and w.accum:

@@ -78,7 +78,8 @@ BAD = [
     ("causal2", dict(causal=2), ft.FA_ERR_INVALID_ARG),
     ("mask_kind", dict(mask_kind=5), ft.FA_ERR_INVALID_ARG),
     ("mask_batch", dict(mask_kind=ft.FA_MASK_ADD_F32, mask_batch=3), ft.FA_ERR_INVALID_ARG),
-    ("reserved", dict(reserved=1), ft.FA_ERR_INVALID_ARG),
+    ("window_negative", dict(window=-1), ft.FA_ERR_INVALID_ARG),
+    ("window_offset_too_big", dict(window=8, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_too_big", dict(causal=1, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_negative", dict(causal=1, q_offset=-1), ft.FA_ERR_INVALID_ARG),
 ]

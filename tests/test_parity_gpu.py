@@ -30,6 +30,18 @@ SMALL = [
     W("bf16_single_query", B=1, Hq=2, Hkv=2, Sq=1, Sk=700, D=128, causal=True, q_offset=699, seed=22),
     W("bf16_long_keys_small_q", B=1, Hq=4, Hkv=1, Sq=64, Sk=5000, D=128, causal=True, q_offset=4936,
       accum=True, seed=23),
+    # a query chunk in the middle of the keys: key tiles past the chunk have no step at all
+    W("bf16_causal_chunk_mid", B=1, Hq=4, Hkv=2, Sq=150, Sk=600, D=128, causal=True, q_offset=100, seed=30),
+    # sliding window (half-width w: |q_offset + i - j| <= w)
+    W("f32_window_offset", B=1, Hq=2, Hkv=1, Sq=70, Sk=150, D=64, dtype="f32", q_offset=40, window=20,
+      seed=31),
+    W("bf16_window_d128_ragged", B=1, Hq=4, Hkv=2, Sq=900, Sk=900, D=128, window=130, seed=32),
+    W("bf16_window_pad_self_d64", B=1, Hq=4, Hkv=2, Sq=700, Sk=700, D=64, window=100, mask="pad_self", seed=33),
+    W("bf16_window_narrow_bool", B=2, Hq=2, Hkv=1, Sq=400, Sk=400, D=128, window=5, mask="random_bool",
+      seed=34),
+    W("bf16_window_causal_accum", B=1, Hq=4, Hkv=1, Sq=300, Sk=1000, D=128, causal=True, q_offset=650,
+      window=200, accum=True, seed=35),
+    W("bf16_window_chunk_mid_d64", B=1, Hq=2, Hkv=2, Sq=200, Sk=900, D=64, q_offset=100, window=64, seed=36),
 ]
 
 
@@ -90,7 +102,7 @@ def test_dk_dv_are_deterministic():
 
 # ---- full-size workloads ------------------------------------------------------------------------
 
-@pytest.mark.parametrize("w", [wl.DIT_SELF, wl.DIT_CROSS], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [wl.DIT_SELF, wl.DIT_SELF_WINDOW, wl.DIT_CROSS], ids=lambda w: w.name)
 def test_full_dit_workloads_match_oracle(w):
     inputs = wl.make_inputs(w)
     got = pu.run_gpu(w, pu.to_device(inputs, w))
