@@ -154,9 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = s.Hq / s.Hkv;
 
-  // ---- work unit: key tile kt of (b, kvh); under the causal rule the low key tiles carry the most work
-  const int kt = blockIdx.x % p.nkt;
-  const int bkv = blockIdx.x / p.nkt;
+  // ---- work unit: key tile kt of (b, kvh). Under the causal rule the low key tiles carry the most
+  //      work, so blocks run key-tile-major: every head's heavy tiles are in the first wave and the
+  //      light ones fill the SMs that free up (longest work first)
+  const int nbkv = s.B * s.Hkv;
+  const int kt = blockIdx.x / nbkv;
+  const int bkv = blockIdx.x % nbkv;
   const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
   const int j0 = kt * kBN;
   const int mb = s.mask_batch > 1 ? b : 0;
