@@ -17,16 +17,21 @@
 //     dV  += P^T dO          (TMEM x SMEM)
 //     dK  += dS^T Q          (TMEM x SMEM)
 //     dQ^T = K^T dS^T  (D = 128)  or  dQ = dS K  (D = 64)   (SMEM x SMEM -> TMEM)
-//     the dQ partial goes TMEM -> SMEM -> fp32 dQ accumulator with one TMA bulk
-//     tensor reduce-add (the add happens in L2).
+//     the dQ partial is added into the fp32 dQ accumulator in L2.
 // Roles: warp 0 TMA (K, V once; Q, dO per step), warp 1 MMA issue + TMEM owner,
 // warp 2 LSE/D staging, warps 4-11 softmax-grad: two warps per TMEM lane quadrant,
-// a thread owns one key and half of the step's query columns; warps 12-15 stage
-// each step's dQ partial (TMEM -> SMEM) and issue its reduce-add. Each 32-column score
-// chunk receives its own P^T (16 columns) and dS^T (16 columns) once read, so no
-// warp writes TMEM another warp still reads. With D = 128 the S/dP TMEM block is
-// double-buffered so the next step's S^T, dP^T run on the tensor core while the
-// softmax-grad warps work on the current one.
+// a thread owns one key and a share of the step's query columns; warps 12-15 move
+// each step's dQ partial out of TMEM and add it into the accumulator. Each 32-column
+// score chunk receives its own P^T (16 columns) and dS^T (16 columns) once read, so no
+// warp writes TMEM another warp still reads.
+//
+// Each step's softmax-grad is split in two rounds of 64 queries; the first round's
+// dV / dK MMAs run while the second round is computed.
+// D = 128: the dQ^T partial goes from TMEM to registers and into the accumulator with
+// coalesced red.add (one 128-byte run of 32 features per warp instruction), so it
+// needs no shared memory, and the Q/dO slot is handed back by the MMA commit after
+// dV / dK have read it. D = 64: the dQ partial is staged in the step's consumed Q/dO
+// slot and added with one TMA bulk tensor reduce-add.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,21 +47,25 @@ using namespace tc;
 
 constexpr int kBN = 128;       // keys per CTA
 constexpr int kThreads = 512;  // 16 warps = 4 warpgroups (128 registers per thread at launch)
-// Register split by warpgroup (setmaxnreg, inside each role's branch): control warps 0-3 keep 80,
-// the softmax-grad warpgroups keep 128, the dQ stager (warps 12-15) takes 176 so it can hold a
-// whole dQ partial row: (80 + 128 + 128 + 176) x 128 = 65536 = 512 x 128.
-constexpr int kRegsControl = 80;
-constexpr int kRegsStager = 176;
-static_assert(kRegsControl + 2 * 128 + kRegsStager <= 4 * 128, "register split exceeds the launch pool");
+// Register split by warpgroup (setmaxnreg, inside each role's branch): control warps 0-3 drop to
+// 64, the softmax-grad warpgroups take 144 (a 32-query chunk of scores and of dP^T at once), the
+// dQ stager (warps 12-15) 160 so it can hold a whole dQ partial row:
+// (64 + 144 + 144 + 160) x 128 = 65536 = 512 x 128.
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 144;
+constexpr int kRegsStager = 160;
+static_assert(kRegsControl + 2 * kRegsSoftmax + kRegsStager <= 4 * 128, "register split exceeds the launch pool");
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BQ = 128;                        // query rows per step (every MMA has N = 128 or D)
-  static constexpr int NBUF = 1;                        // one S/dP TMEM block
-  static constexpr int BUF_COLS = 2 * BQ;               // S^T [0,BQ), dP^T [BQ,2BQ)
+  static constexpr bool RED_DQ = D == 128;              // dQ partial added from registers with red.add
+  static constexpr int BQ = 128;                        // query rows per step (N = 128 MMAs)
+  static constexpr int NBUF = 1;                        // S/dP TMEM blocks
+  static constexpr int BUF_COLS = 2 * BQ;               // block b: S^T [b*2BQ, +BQ), dP^T [b*2BQ+BQ, +BQ)
   static constexpr int NCHUNK = BQ / 32;                // 32-column score chunks per step
   static constexpr int CHUNKS_PER_WARP = NCHUNK / 2;    // two warps per lane quadrant
+  static constexpr bool TWO_ROUND = CHUNKS_PER_WARP == 2;   // the first 64 queries' dV / dK go early
   // chunk c of the scores (columns [32c, 32c+32)) is overwritten by P^T at [32c, 32c+16)
   // and dS^T at [32c+16, 32c+32) (bf16 pairs) once it has been read
   static constexpr int DQ_COL = BQ;                     // dQ^T (D=128) / dQ (D=64) over the dP^T block
@@ -65,6 +74,7 @@ struct BwdCfg {
   static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
   static constexpr int DQ_CHUNKS = (DQ_TRANSPOSED ? BQ : D) / 32;   // 32-column TMEM chunks of the dQ partial
   static constexpr int NSTAGE = 2;                      // Q/dO ring depth
+  static constexpr int NDS = 1;                         // dS^T shared-memory buffers
   // shared memory (bytes)
   static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
   static constexpr int KV_TILE = kBN * D * 2;
@@ -77,11 +87,12 @@ struct BwdCfg {
   // [NSTAGE] x (Q, dO); once dV/dK of a step have read its slot, the slot holds that step's
   // fp32 dQ partial ([BQ][D] = 2 * Q_TILE bytes) until the reduce-add has read it
   static constexpr int OFF_STAGE = 2 * KV_TILE;
-  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // dS^T (the B / A operand of the dQ MMA)
-  static constexpr int OFF_LSED = OFF_DS + DS_TILE;                // [NSTAGE] x (lse2[BQ], dsum[BQ])
+  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // [NDS] x dS^T (operand of the dQ MMA)
+  static constexpr int OFF_LSED = OFF_DS + NDS * DS_TILE;          // [NSTAGE] x (lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
-  static constexpr int BYTES = OFF_BAR + 256;
-  static_assert(BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
+  static constexpr int BYTES = OFF_BAR + 512;
+  static_assert(RED_DQ || BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
+  static_assert(NBUF * BUF_COLS + 2 * D <= 512, "TMEM columns");
   static_assert(BYTES <= 232448, "shared memory per block");
 };
 
@@ -143,8 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_p_half = bar_p_full + C::NBUF;          // 1: P^T / dS^T of the step's first 64 queries
   uint64_t* bar_dq_full = bar_p_half + 1;               // NBUF
   uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
-  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // 1: the dQ MMA has read dS^T
-  uint64_t* bar_mma_done = bar_ds_free + 1;             // 1
+  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // NDS: the dQ MMA has read that dS^T buffer
+  uint64_t* bar_mma_done = bar_ds_free + C::NDS;        // 1
   uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 4 stager warps filled the dQ staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_stage_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_dq_full[i], 1);
       mbar_init(&bar_dq_free[i], 4);
     }
-    mbar_init(bar_ds_free, 1);
+    for (int i = 0; i < C::NDS; ++i) mbar_init(&bar_ds_free[i], 1);
     mbar_init(bar_p_half, 8);
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_stage_full, 4);
@@ -256,64 +267,72 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // Base descriptors per operand tile; every k-step adds a compile-time byte offset (desc_add).
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dKmn = smem_desc_sw128(sK, C::KV_BOX, 1024);   // K as an MN-major operand
-      // S^T of step st: the score block's previous contents (P^T, dS^T of step st-1) were
-      // consumed by the dV / dK MMAs issued before (tcgen05 MMAs of a thread run in order)
+      // S^T of step st into score block st % NBUF: the block's previous contents (P^T, dS^T of
+      // step st - NBUF) were consumed by the dV / dK MMAs issued before (tcgen05 MMAs of a
+      // thread run in order)
       auto issue_st = [&](int st) {
         const int slot = st % C::NSTAGE;
         tc_fence_after();
+        const uint32_t tb = tmem + (st % C::NBUF) * C::BUF_COLS;
         const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tmem, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
+          mma_ss(tb, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
                  idesc_s, k > 0);
       };
-      // dP^T of step st: its TMEM block held the dQ partial of step st-1, drained by the stager
+      // dP^T of step st: its TMEM block held the dQ partial of step st - NBUF, drained by the stager
       auto issue_dp = [&](int st) {
         const int slot = st % C::NSTAGE;
         tc_fence_after();
+        const uint32_t tb = tmem + (st % C::NBUF) * C::BUF_COLS;
         const uint64_t ddo0 =
             smem_desc_sw128(smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE) + C::Q_TILE, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tmem + BQ, desc_add(dV0, (k / 4) * C::KV_BOX + (k % 4) * 32),
+          mma_ss(tb + BQ, desc_add(dV0, (k / 4) * C::KV_BOX + (k % 4) * 32),
                  desc_add(ddo0, (k / 4) * C::QBOX + (k % 4) * 32), idesc_s, k > 0);
-        mma_commit(&bar_sdp_full[0]);
+        mma_commit(&bar_sdp_full[st % C::NBUF]);
       };
-      // dV, dK over the step's queries [64h, 64h + 64): k-step k covers queries [16k, 16k+16),
-      // score chunk k/2, columns (k%2)*8 within its P^T / dS^T half
+      // dV, dK over the step's queries [64h, 64h + 64) (all BQ queries when BQ = 64): k-step k
+      // covers queries [16k, 16k+16), score chunk k/2, columns (k%2)*8 within its P^T / dS^T half
       auto issue_dvdk = [&](int st, int h) {
         const int slot = st % C::NSTAGE;
         tc_fence_after();
+        const uint32_t tb = tmem + (st % C::NBUF) * C::BUF_COLS;
         const uint32_t sq = smem_u32(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
         const uint64_t dqmn = smem_desc_sw128(sq, C::QBOX, 1024), ddomn = smem_desc_sw128(sq + C::Q_TILE, C::QBOX, 1024);
+        constexpr int KS = C::TWO_ROUND ? BQ / 32 : BQ / 16;   // k-steps per call
 #pragma unroll
-        for (int kk = 0; kk < BQ / 32; ++kk) {
-          const int k = h * (BQ / 32) + kk;
-          mma_ts(tmem + C::DV_COL, tmem + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
+        for (int kk = 0; kk < KS; ++kk) {
+          const int k = h * KS + kk;
+          mma_ts(tmem + C::DV_COL, tb + 32 * (k / 2) + (k % 2) * 8, desc_add(ddomn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < BQ / 32; ++kk) {
-          const int k = h * (BQ / 32) + kk;
-          mma_ts(tmem + C::DK_COL, tmem + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
+        for (int kk = 0; kk < KS; ++kk) {
+          const int k = h * KS + kk;
+          mma_ts(tmem + C::DK_COL, tb + 32 * (k / 2) + 16 + (k % 2) * 8, desc_add(dqmn, k * 2048), idesc_g,
                  (st > 0 || k > 0) ? 1u : 0u);
         }
       };
-      // dQ of step st (all of its dS^T is in shared memory)
+      // dQ of step st (all of its dS^T is in shared memory), over the step's dP^T columns
       auto issue_dq = [&](int st) {
-        const uint64_t ds0 = smem_desc_sw128(smem_u32(smem + C::OFF_DS), C::DS_BLOCK, 1024);
+        const uint32_t tb = tmem + (st % C::NBUF) * C::BUF_COLS;
+        const uint64_t ds0 =
+            smem_desc_sw128(smem_u32(smem + C::OFF_DS + (st % C::NDS) * C::DS_TILE), C::DS_BLOCK, 1024);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           if (C::DQ_TRANSPOSED)
-            mma_ss(tmem + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
+            mma_ss(tb + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
           else
-            mma_ss(tmem + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
+            mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
         }
-        mma_commit(&bar_dq_full[0]);
-        mma_commit(bar_ds_free);
+        mma_commit(&bar_dq_full[st % C::NBUF]);
+        mma_commit(&bar_ds_free[st % C::NDS]);
       };
 
-      // Issue whichever MMA group is ready; none that waits holds back one that is ready:
+      // Issue whichever MMA group is ready; none that waits holds back one that is ready. With one
+      // S/dP block (D = 64):
       //   dV/dK of step ns, first 64 queries: once their P^T / dS^T are written;
       //   dV/dK of the other 64 queries and dQ of step ns: once all of its P^T / dS^T are written;
       //   dP^T of step np: after S^T(np) and once the stager drained the dQ partial of step np-1;
@@ -337,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           progressed = true;
         } else if (na > ns && mbar_test(&bar_p_full[0], ns & 1)) {
           issue_dvdk(ns, 1);
+          if (C::RED_DQ) mma_commit(&bar_qdo_empty[ns % C::NSTAGE]);   // dV / dK were the slot's last readers
           issue_dq(ns++);
           progressed = true;
         } else if (np < nt && (np == 0 || mbar_test(&bar_dq_free[0], (np - 1) & 1))) {
@@ -385,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
    }
   } else if (warp < 12) {
+    regs_inc<kRegsSoftmax>();
     // ---------------------------------------------------------------- softmax-grad
     const int wq = warp & 3;                      // TMEM lane quadrant
     const int half = (warp - 4) >> 2;             // which half of the step's query columns
@@ -408,10 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     bool ok = true;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
-      const int buf = 0, slot = st % C::NSTAGE;
-      ok = mbar_wait(&bar_sdp_full[0], st & 1, abort_flag, p.status, 130);
+      const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st % C::NDS;
+      ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
-      if (st >= 1) ok = ok && mbar_wait(bar_ds_free, (st - 1) & 1, abort_flag, p.status, 132);
+      if (st >= C::NDS) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - C::NDS) / C::NDS) & 1, abort_flag, p.status, 132);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
@@ -420,21 +441,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // every pair of this step visible for this key: open tile, real key, all BQ rows inside the
       // key's row band (which also ends at the last real row)
       const bool full = code == TILE_OPEN && key_ok && it.i0 >= row_lo && (long long)it.i0 + BQ - 1 <= row_hi;
-      const uint32_t sds = smem_u32(smem + C::OFF_DS) + r * 128;
+      const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE) + r * 128;
 #pragma unroll
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
         // round cc covers queries [64cc, 64cc + 64): the two warps of a lane quadrant take one
         // 32-query chunk each, and the first round is handed to the dV / dK MMAs right away
         const int c = cc * 2 + half;   // score chunk: queries [32c, 32c+32)
-        // the whole score chunk first (its upper half receives dS^T below), then dP^T / LSE / D
-        // 16 queries at a time
-        uint32_t sr[32];
+        // the chunk's scores and dP^T in one go (one TMEM round trip; the score columns then
+        // receive P^T and dS^T), LSE / D 16 queries at a time
+        uint32_t sr[32], dr[32];
         tmem_ld32(tb + c * 32, sr);
+        tmem_ld32(tb + BQ + c * 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           const int q0 = c * 32 + sub * 16;   // first query of these 16
-          uint32_t dr[16];
-          tmem_ld16(tb + BQ + q0, dr);
           float l2[16], dv_[16];
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
@@ -443,9 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
             dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
           }
-          tmem_wait_ld();
-          if (sub == 0) reg_fence(sr);
-          reg_fence16(dr);
           float pv[16];
           if (full) {
 #pragma unroll
@@ -487,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-            dk8[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[2 * e]) - dv_[2 * e]),
-                                 pv[2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dv_[2 * e + 1]));
+            dk8[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[sub * 16 + 2 * e]) - dv_[2 * e]),
+                                 pv[2 * e + 1] * (__uint_as_float(dr[sub * 16 + 2 * e + 1]) - dv_[2 * e + 1]));
           }
           // P^T and dS^T of these 16 queries over this chunk's own (already read) score columns
           tmem_st8(tb + c * 32 + sub * 8, pk);
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                          dk8[4 * u + 2], dk8[4 * u + 3]);
           }
         }
-        if (cc == 0) {
+        if (C::TWO_ROUND && cc == 0) {
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
@@ -572,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else {
     regs_inc<kRegsStager>();
     // ---------------------------------------------------------------- dQ stager (warps 12-15)
-    // Each step's dQ partial: TMEM -> SMEM [BQ][D] fp32 -> dQ accumulator with one TMA
-    // reduce-add (the add happens in L2) issued by the leader thread.
+    // Each step's dQ partial leaves TMEM for the fp32 dQ accumulator, where the add happens in
+    // L2: D = 128 from registers with red.add, D = 64 through SMEM [BQ][D] and one TMA reduce-add
+    // issued by the leader thread.
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
@@ -582,32 +603,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     int st = 0;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
-      const int slot = st % C::NSTAGE;
+      const int slot = st % C::NSTAGE, buf = st % C::NBUF;
       float* sdq = reinterpret_cast<float*>(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
       const uint32_t sbase = smem_u32(sdq);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[0], st & 1, abort_flag, p.status, 134))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 134)))
+        break;
       // the whole dQ partial row of this thread into registers, so the TMEM block is released at once
       tc_fence_after();
       uint32_t v[C::DQ_CHUNKS][32];
 #pragma unroll
-      for (int c = 0; c < C::DQ_CHUNKS; ++c) tmem_ld32(tmem + C::DQ_COL + c * 32 + lane_off, v[c]);
+      for (int c = 0; c < C::DQ_CHUNKS; ++c)
+        tmem_ld32(tmem + buf * C::BUF_COLS + C::DQ_COL + c * 32 + lane_off, v[c]);
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < C::DQ_CHUNKS; ++c) reg_fence(v[c]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dq_free[0]);   // the TMEM block is free for the next dP^T
-      // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read
+      if (lane == 0) mbar_arrive(&bar_dq_free[buf]);   // the TMEM block is free for the next dP^T
+      if constexpr (C::RED_DQ) {
+        // thread = feature d, registers = queries 32c + e: each warp instruction adds one 128-byte
+        // run of 32 consecutive features of one query row (rows past Sq are not touched)
+        const int d = wq * 32 + lane;
+        const int nrows = min(BQ, s.Sq - it.i0);
+        float* dst = p.dq_acc + ((size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq + it.i0) * D + d;
 #pragma unroll
-      for (int c = 0; c < C::DQ_CHUNKS; ++c) {
-        if (C::DQ_TRANSPOSED) {
-          // thread = feature d, registers = queries 32c + e: row-major [q][d], lanes on consecutive d
-          const int d = wq * 32 + lane;
+        for (int c = 0; c < C::DQ_CHUNKS; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) st_shared_f32(sbase + ((c * 32 + e) * D + d) * 4, __uint_as_float(v[c][e]));
-        } else {
-          // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
-          const int q = wq * 32 + lane;
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < nrows) red_add_f32(dst + (size_t)(c * 32 + e) * D, __uint_as_float(v[c][e]));
+        }
+      } else {
+        // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read:
+        // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
+        static_assert(!C::DQ_TRANSPOSED, "the staged path takes dQ with query rows on TMEM lanes");
+        const int q = wq * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < C::DQ_CHUNKS; ++c) {
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int cidx = (u + lane) & 7;
@@ -615,24 +646,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                          v[c][4 * cidx + 2], v[c][4 * cidx + 3]);
           }
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_stage_full);
-      // the leader waits for all four warps' stores, issues the reduce, and hands the slot back to
-      // the producer once the reduce has read it; its warp leaves the loop together on a timeout
-      bool filled = true;
-      if (leader) filled = mbar_wait(bar_stage_full, st & 1, abort_flag, p.status, 136);
-      if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
-      if (leader) {
-        tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, b * s.Hq + kvh * G + it.hh);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(&bar_qdo_empty[slot]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_stage_full);
+        // the leader waits for all four warps' stores, issues the reduce, and hands the slot back to
+        // the producer once the reduce has read it; its warp leaves the loop together on a timeout
+        bool filled = true;
+        if (leader) filled = mbar_wait(bar_stage_full, st & 1, abort_flag, p.status, 136);
+        if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
+        if (leader) {
+          tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, b * s.Hq + kvh * G + it.hh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bar_qdo_empty[slot]);
+        }
       }
       ++st;
     }
-    if (leader) bulk_wait_group0();
+    if (!C::RED_DQ && leader) bulk_wait_group0();
   }
 
   tc_fence_before();

@@ -130,8 +130,9 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-__device__ __forceinline__ void st_shared_f32(uint32_t saddr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(v) : "memory");
+// Fire-and-forget fp32 add into global memory (performed in L2).
+__device__ __forceinline__ void red_add_f32(float* ptr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
