@@ -235,9 +235,17 @@ fa_status fa_train_fwd(const fa_params* p, const void* q, const void* k, const v
   return cuda_status(e, "forward launch");
 }
 
+// Rows of the accumulator written back out by the fused SET_ROWS backward (n_rows == 0: none).
+struct RowsOut {
+  long long begin = 0;
+  int n = 0;
+  void* dk = nullptr;
+  void* dv = nullptr;
+};
+
 static fa_status bwd_common(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
                             const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                            bool accum, void* ws, size_t ws_bytes, void* stream) {
+                            bool accum, void* ws, size_t ws_bytes, void* stream, const RowsOut& rb = RowsOut{}) {
   Shape s;
   fa_status st = check_params(p, s);
   if (st != FA_OK) return st;
@@ -247,21 +255,38 @@ static fa_status bwd_common(const fa_params* p, const void* q, const void* k, co
                      {mask, mask_bytes(s), "mask"}, {o, q_bytes(s), "o"}, {lse, rows * 4, "lse"},
                      {dO, q_bytes(s), "dO"}};
   const size_t gk = accum ? kv_bytes(s, 4) : kv_bytes(s, es);
-  const Span out[] = {{dq, q_bytes(s), "dq"}, {dk, gk, accum ? "dk_acc" : "dk"}, {dv, gk, accum ? "dv_acc" : "dv"}};
-  if ((st = check_buffers(in, 7, out, 3)) != FA_OK) return st;
+  if (rb.n < 0 || rb.begin < 0 || rb.begin + rb.n > s.Sk) {
+    set_error("rows [%lld, %lld) outside the %d keys", rb.begin, rb.begin + rb.n, s.Sk);
+    return FA_ERR_INVALID_ARG;
+  }
+  const size_t gr = (size_t)s.B * s.Hkv * rb.n * s.D * es;
+  const Span out[] = {{dq, q_bytes(s), "dq"}, {dk, gk, accum ? "dk_acc" : "dk"}, {dv, gk, accum ? "dv_acc" : "dv"},
+                      {rb.dk, gr, "dk_rows"}, {rb.dv, gr, "dv_rows"}};
+  const int n_out = rb.n > 0 ? 5 : 3;
+  if ((st = check_buffers(in, 7, out, n_out)) != FA_OK) return st;
   const BwdPlan plan = plan_bwd(s);
-  const Span all[] = {in[0], in[1], in[2], in[3], in[4], in[5], in[6], out[0], out[1], out[2]};
-  if ((st = check_ws(ws, ws_bytes, plan.total, all, 10)) != FA_OK) return st;
+  const Span all[] = {in[0], in[1], in[2], in[3], in[4], in[5], in[6], out[0], out[1], out[2], out[3], out[4]};
+  if ((st = check_ws(ws, ws_bytes, plan.total, all, 7 + n_out)) != FA_OK) return st;
 
   cudaStream_t cs = (cudaStream_t)stream;
   if (s.Sq == 0) {
-    // No query rows: the gradient of every key is zero.
-    if (accum) return FA_OK;
+    // No query rows: the gradient of every key is zero (the accumulator keeps its contents,
+    // and the read-back rows are those contents).
+    if (accum) {
+      if (rb.n == 0) return FA_OK;
+      cudaError_t e = launch_rows_copy(s, static_cast<const float*>(dk), static_cast<const float*>(dv), rb.begin,
+                                       rb.n, rb.dk, rb.dv, cs);
+      return cuda_status(e, "rows read-back");
+    }
     cudaError_t e = cudaMemsetAsync(dk, 0, gk, cs);
     if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, gk, cs);
     return cuda_status(e, "zero dK/dV");
   }
   BwdArgs a{s, q, k, v, mask, o, lse, dO, dq, dk, dv, accum, cs};
+  a.rows_begin = rb.begin;
+  a.n_rows = rb.n;
+  a.dk_rows = rb.dk;
+  a.dv_rows = rb.dv;
   cudaError_t e = plan.tensor_core ? tc_bwd(a, plan, (char*)ws)
                                    : simt_bwd(a, reinterpret_cast<float*>((char*)ws + plan.dsum_off));
   return cuda_status(e, "backward launch");
@@ -277,6 +302,44 @@ fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const void* k, c
                              const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
                              float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
   return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream);
+}
+
+fa_status fa_train_bwd_accum_rows(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
+                                  const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
+                                  float* dv_acc, int64_t rows_begin, int32_t n_rows, void* dk_rows, void* dv_rows,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  RowsOut rows;
+  rows.begin = rows_begin;
+  rows.n = n_rows;
+  rows.dk = dk_rows;
+  rows.dv = dv_rows;
+  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream, rows);
+}
+
+fa_status fa_set_rows_backward(const float* acc, int32_t B, int32_t H, int32_t S, int32_t D, const int64_t* idx,
+                               int32_t n_rows, void* out, int32_t out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (B < 1 || H < 1 || S < 1 || (long long)B * H > 0x7fffffffLL) {
+    set_error("B=%d, H=%d, S=%d: each must be >= 1", B, H, S);
+    return FA_ERR_INVALID_ARG;
+  }
+  if (D < 4 || D > 1024 || D % 4 != 0) { set_error("D=%d: a multiple of 4 in [4, 1024]", D); return FA_ERR_INVALID_ARG; }
+  if (n_rows < 0) { set_error("n_rows=%d must be >= 0", n_rows); return FA_ERR_INVALID_ARG; }
+  if (out_dtype != FA_F32 && out_dtype != FA_BF16) { set_error("out_dtype=%d invalid", out_dtype); return FA_ERR_INVALID_ARG; }
+  if (n_rows == 0) return FA_OK;
+  if (acc == nullptr || idx == nullptr || out == nullptr) { set_error("acc, idx and out must be non-NULL"); return FA_ERR_INVALID_ARG; }
+  if ((uintptr_t)acc % 16 != 0 || (uintptr_t)out % 16 != 0 || (uintptr_t)idx % 8 != 0) {
+    set_error("acc and out must be 16-byte aligned, idx 8-byte aligned");
+    return FA_ERR_INVALID_ARG;
+  }
+  const size_t heads = (size_t)B * H;
+  const Span in[] = {{acc, heads * S * D * 4, "acc"}, {idx, (size_t)n_rows * 8, "idx"}};
+  const Span outs[] = {{out, heads * n_rows * D * (out_dtype == FA_BF16 ? 2 : 4), "out"}};
+  for (const Span& a : in)
+    if (overlaps(outs[0], a)) { set_error("out overlaps %s", a.name); return FA_ERR_INVALID_ARG; }
+  return cuda_status(launch_set_rows_backward(acc, (int)heads, S, D, idx, n_rows, out, out_dtype,
+                                              device_status_ptr(), (cudaStream_t)stream),
+                     "set_rows backward launch");
 }
 
 fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream) {

@@ -49,6 +49,12 @@ struct BwdArgs {
   void* dv;
   bool accum;
   cudaStream_t stream;
+  // accumulate only: keys [rows_begin, rows_begin + n_rows) are also written, after the add, to
+  // dk_rows / dv_rows [B, Hkv, n_rows, D] in dtype (n_rows == 0: none)
+  long long rows_begin = 0;
+  int n_rows = 0;
+  void* dk_rows = nullptr;
+  void* dv_rows = nullptr;
 };
 
 // Carve-up of the caller's workspace. Offsets are 256-byte aligned.
@@ -97,6 +103,14 @@ cudaError_t simt_bwd(const BwdArgs& a, float* dsum);
 cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero);
 cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc);
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
+
+// SET_ROWS backward gather (fa_set_rows_backward): out[bh, r, :] = acc[bh, idx[r], :].
+constexpr unsigned kSiteRowIndex = 950;
+cudaError_t launch_set_rows_backward(const float* acc, int heads, int S, int D, const int64_t* idx, int n_rows,
+                                     void* out, int out_dtype, unsigned* status, cudaStream_t st);
+// The same gather for the contiguous keys [row0, row0 + n_rows) of dK / dV accumulators (in s.dtype).
+cudaError_t launch_rows_copy(const Shape& s, const float* dk_acc, const float* dv_acc, long long row0, int n_rows,
+                             void* dk_rows, void* dv_rows, cudaStream_t st);
 
 // tcgen05 paths (bf16, D in {64, 128}).
 bool tc_fwd_supported(const Shape& s);

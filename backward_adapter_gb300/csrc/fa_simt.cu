@@ -119,7 +119,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(
     Shape s, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const void* mask,
     const float* __restrict__ lse, const T* __restrict__ dO, const float* __restrict__ dsum, void* dk_out,
-    void* dv_out, bool accum) {
+    void* dv_out, bool accum, long long rows_begin, int n_rows, T* dk_rows, T* dv_rows) {
   constexpr int KT = 32, QT = 32, DP = D + 1, NT = D / 32, KPW = KT / 8;
   extern __shared__ float smem_dkdv[];
   float (*Qs)[DP] = reinterpret_cast<float (*)[DP]>(smem_dkdv);
@@ -205,13 +205,22 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(
     const int j = j0 + warp * KPW + kk;
     if (j >= s.Sk) continue;
     const size_t base = ((size_t)(b * s.Hkv + kvh) * s.Sk + j) * D;
+    // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
+    const long long rr = (long long)j - rows_begin;
+    const bool read_back = accum && rr >= 0 && rr < n_rows;
+    const size_t rbase = ((size_t)(b * s.Hkv + kvh) * n_rows + (read_back ? rr : 0)) * D;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const size_t idx = base + lane + 32 * t;
       const float gk = dk[kk][t] * s.scale, gv = dv[kk][t];
       if (accum) {
-        static_cast<float*>(dk_out)[idx] += gk;
-        static_cast<float*>(dv_out)[idx] += gv;
+        const float nk = static_cast<float*>(dk_out)[idx] + gk, nv = static_cast<float*>(dv_out)[idx] + gv;
+        static_cast<float*>(dk_out)[idx] = nk;
+        static_cast<float*>(dv_out)[idx] = nv;
+        if (read_back) {
+          from_f(dk_rows + rbase + lane + 32 * t, nk);
+          from_f(dv_rows + rbase + lane + 32 * t, nv);
+        }
       } else {
         from_f(static_cast<T*>(dk_out) + idx, gk);
         from_f(static_cast<T*>(dv_out) + idx, gv);
@@ -340,7 +349,8 @@ cudaError_t simt_bwd_t(const BwdArgs& a, const float* dsum) {
   if ((e = prof_begin(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
   bwd_dkdv_simt_kernel<T, D><<<g1, kThreads, sm1, a.stream>>>(s, (const T*)a.q, (const T*)a.k, (const T*)a.v,
                                                             a.mask, a.lse, (const T*)a.dO, dsum, a.dk, a.dv,
-                                                            a.accum);
+                                                            a.accum, a.rows_begin, a.accum ? a.n_rows : 0,
+                                                            (T*)a.dk_rows, (T*)a.dv_rows);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2((s.Sq + 31) / 32, s.Hq, s.B);

@@ -107,6 +107,10 @@ struct BwdTcParams {
   void* dk;  // bf16 [B,Hkv,Sk,D], or fp32 accumulator
   void* dv;
   int accum;
+  long long rows_begin;   // accumulate: keys [rows_begin, rows_begin + n_rows) are also written, after
+  int n_rows;             // the add, to dk_rows / dv_rows (bf16 [B, Hkv, n_rows, D])
+  __nv_bfloat16* dk_rows;
+  __nv_bfloat16* dv_rows;
   int nqt, nkt;
   unsigned* status;
 };
@@ -546,6 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     tc_fence_after();
     if (ok) {
       const size_t row = ((size_t)(b * s.Hkv + kvh) * s.Sk + (key_ok ? j : 0)) * D;
+      // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
+      const long long rr = (long long)j - p.rows_begin;
+      const bool read_back = p.accum && key_ok && rr >= 0 && rr < p.n_rows;
+      const size_t rrow = ((size_t)(b * s.Hkv + kvh) * p.n_rows + (read_back ? rr : 0)) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float mul = which == 0 ? 1.f : s.scale;
@@ -566,14 +574,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           if (!key_ok) continue;
           if (p.accum) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(outp) + row + c * 32);
+            // all eight loads first (the read-back stores below could alias them as far as the
+            // compiler knows), then the adds and the stores
+            float4 a[8];
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) a[v4] = dst[v4];
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4) {
-              float4 a = dst[v4];
-              a.x += __uint_as_float(v[4 * v4]) * mul;
-              a.y += __uint_as_float(v[4 * v4 + 1]) * mul;
-              a.z += __uint_as_float(v[4 * v4 + 2]) * mul;
-              a.w += __uint_as_float(v[4 * v4 + 3]) * mul;
-              dst[v4] = a;
+              a[v4].x += __uint_as_float(v[4 * v4]) * mul;
+              a[v4].y += __uint_as_float(v[4 * v4 + 1]) * mul;
+              a[v4].z += __uint_as_float(v[4 * v4 + 2]) * mul;
+              a[v4].w += __uint_as_float(v[4 * v4 + 3]) * mul;
+              dst[v4] = a[v4];
+            }
+            if (read_back) {
+              uint2* rdst = reinterpret_cast<uint2*>((which == 0 ? p.dv_rows : p.dk_rows) + rrow + c * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                rdst[v4] = make_uint2(pack_bf16x2(a[v4].x, a[v4].y), pack_bf16x2(a[v4].z, a[v4].w));
             }
           } else {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outp) + row + c * 32);
@@ -708,6 +726,10 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   p.dk = a.dk;
   p.dv = a.dv;
   p.accum = a.accum ? 1 : 0;
+  p.rows_begin = a.rows_begin;
+  p.n_rows = a.accum ? a.n_rows : 0;
+  p.dk_rows = static_cast<__nv_bfloat16*>(a.dk_rows);
+  p.dv_rows = static_cast<__nv_bfloat16*>(a.dv_rows);
   p.status = status;
   const int smem = C::BYTES;
   if ((e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)

@@ -23,7 +23,8 @@ FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
-            "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc", "fa_train_selftest_wait")
+            "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc", "fa_train_selftest_wait",
+            "fa_set_rows_backward", "fa_train_bwd_accum_rows")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -78,6 +79,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_train_selftest_wait.restype = st
     lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_device_status.restype = st
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    lib.fa_set_rows_backward.argtypes = [vp, i32, i32, i32, i32, vp, i32, vp, i32, vp]
+    lib.fa_set_rows_backward.restype = st
+    lib.fa_train_bwd_accum_rows.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, sz, vp]
+    lib.fa_train_bwd_accum_rows.restype = st
     _lib = lib
     return lib
 
@@ -219,6 +225,48 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
                                   _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
                                   _stream(q.device, stream)))
     return dq
+
+
+def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows: int, mask=None, *, scale=None,
+                   causal=False, q_offset=None, window=0, dq=None, dk_rows=None, dv_rows=None, workspace=None,
+                   stream=None):
+    """Accumulating backward fused with the SET_ROWS backward of keys [rows_begin, rows_begin + n_rows).
+
+    Adds dK/dV into dk_acc/dv_acc and also returns those keys' finished sums, read back in q's
+    dtype: (dQ, dK_rows [B, Hkv, n_rows, D], dV_rows [B, Hkv, n_rows, D]).
+    """
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
+    if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
+        raise TypeError("dk_acc and dv_acc must be float32")
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    dq = torch.empty_like(q) if dq is None else dq
+    shape = (k.shape[0], k.shape[1], int(n_rows), k.shape[3])
+    dk_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dk_rows is None else dk_rows
+    dv_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dv_rows is None else dv_rows
+    ws_bytes = bwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    _check(lib.fa_train_bwd_accum_rows(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                       _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), int(rows_begin), int(n_rows),
+                                       _ptr(dk_rows), _ptr(dv_rows), _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    return dq, dk_rows, dv_rows
+
+
+def set_rows_backward(acc: torch.Tensor, idx: torch.Tensor, out_dtype=torch.bfloat16, out=None, stream=None):
+    """SET_ROWS backward: out[b, h, r] = acc[b, h, idx[r]] (acc fp32 [B, H, S, D], idx int64 [n])."""
+    _need_cuda(acc, idx)
+    if acc.dtype != torch.float32 or acc.dim() != 4:
+        raise TypeError("acc must be float32 [B, H, S, D]")
+    if idx.dtype != torch.int64 or idx.dim() != 1:
+        raise TypeError("idx must be int64 [n_rows]")
+    B, H, S, D = acc.shape
+    if out is None:
+        out = torch.empty((B, H, idx.shape[0], D), dtype=out_dtype, device=acc.device)
+    _need_cuda(out)
+    _check(load_library().fa_set_rows_backward(_ptr(acc), B, H, S, D, _ptr(idx), idx.shape[0], _ptr(out),
+                                               _dtype_code(out), _stream(acc.device, stream)))
+    return out
 
 
 def profile_set_events(kernel: int, start=None, stop=None) -> None:

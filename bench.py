@@ -2,8 +2,9 @@
 """Benchmark of the fused flash-attention training step on GB300.
 
 One step = the whole op over one batch of seeded synthetic input: forward
-(O, LSE) then backward (D precompute, dQ/dK/dV, dQ convert; the accumulating
-variant for workloads that accumulate dK/dV). Throughput is mask- and
+(O, LSE) then backward (D precompute, dQ/dK/dV, dQ convert). Workloads that
+accumulate dK/dV run the accumulating variant, which also reads the chunk's own
+K/V rows back out of the accumulator in the same kernel. Throughput is mask- and
 causal-aware TFLOP/s: 4*D flops per visible (query head, query, key) triple in
 the forward and 10*D in the backward; skipped or masked pairs are not counted.
 
@@ -263,6 +264,11 @@ def run_ours(args):
     if w.accum:
         dk = torch.from_numpy(inputs["dk_acc"]).to(dev)
         dv = torch.from_numpy(inputs["dv_acc"]).to(dev)
+        # the chunk's own K/V rows (the last Sq keys of the window) are read back from the
+        # accumulator in the same kernel (fused SET_ROWS backward)
+        rows_shape = (w.B, w.Hkv, w.Sq, w.D)
+        dk_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
+        dv_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
     else:
         dk, dv = torch.empty_like(d["k"]), torch.empty_like(d["v"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -270,8 +276,8 @@ def run_ours(args):
     def step(src):
         ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=o, lse=lse, workspace=ws_f, **kw)
         if w.accum:
-            ft.bwd_accum(src["q"], src["k"], src["v"], o, lse, src["do"], dk, dv, src.get("mask"), dq=dq,
-                         workspace=ws_b, **kw)
+            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o, lse, src["do"], dk, dv, w.q_offset, w.Sq,
+                              src.get("mask"), dq=dq, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
         else:
             ft.bwd(src["q"], src["k"], src["v"], o, lse, src["do"], src.get("mask"), dq=dq, dk=dk, dv=dv,
                    workspace=ws_b, **kw)
@@ -380,8 +386,8 @@ def run_ours(args):
                           workspace=ws_f, **kw)
         dq_, dk_, dv_ = outs[sl]
         if w.accum:
-            ft.bwd_accum(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, src.get("mask"), dq=dq_,
-                         workspace=ws_b, **kw)
+            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, w.q_offset, w.Sq,
+                              src.get("mask"), dq=dq_, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
         else:
             ft.bwd(src["q"], src["k"], src["v"], o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
                    workspace=ws_b, **kw)
@@ -421,6 +427,7 @@ def run_ours(args):
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask, "accum": w.accum,
+                   "rows_read_back": [w.q_offset, w.Sq] if w.accum else None,
                    "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
                    "l2": "flushed (256 MiB write) between timed steps, outside the step events",
                    "parallelism": f"replicas x{world}"},

@@ -136,6 +136,42 @@ FA_API fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const voi
                              void* stream);
 
 /*
+ * SET_ROWS backward: the gradient of the rows a chunk wrote into its cached K/V window
+ * (llama.cpp PR #57, commit 2394a4c: the written source's gradient is the result's
+ * gradient at the written rows; the destination, a cache, carries none). With the
+ * window's dL/dK or dL/dV accumulated in `acc`, this reads the written rows back out:
+ *     out[b, h, r, :] = acc[b, h, idx[r], :]      for r < n_rows,
+ * converted to out_dtype (fa_dtype; bf16 rounds to nearest even). acc: fp32 [B, H, S, D];
+ * idx: int64 [n_rows] (device memory, shared by every (b, h); repeats allowed); out:
+ * [B, H, n_rows, D] in out_dtype. D must be a multiple of 4 in [4, 1024]; acc and out
+ * 16-byte aligned, idx 8-byte aligned; out must not overlap acc or idx. An index outside
+ * [0, S) cannot be checked before launch: that row of out is written as zeros and
+ * 0x40000000 | 950 is recorded in the status word read by fa_device_status().
+ * n_rows == 0 is a no-op. Asynchronous on `stream`.
+ */
+FA_API fa_status fa_set_rows_backward(const float* acc, int32_t B, int32_t H, int32_t S, int32_t D,
+                                      const int64_t* idx, int32_t n_rows, void* out, int32_t out_dtype,
+                                      void* stream);
+
+/*
+ * Accumulating backward fused with the SET_ROWS backward of the chunk's own rows: as
+ * fa_train_bwd_accum, and in the same kernel, once a key row's dK/dV sum is complete in
+ * dk_acc/dv_acc, the keys rows_begin .. rows_begin + n_rows - 1 are also written, in the
+ * input dtype p->dtype, to dk_rows / dv_rows [B, Hkv, n_rows, D]:
+ *     dk_rows[b, h, r, :] = dk_acc[b, h, rows_begin + r, :] (after the add), likewise dv.
+ * This is the chunk's K/V gradient read back from the window accumulator (the exact walk of
+ * PR #57 writes the chunk's K/V at the end of the cached window: rows_begin = q_offset,
+ * n_rows = Sq). Needs 0 <= rows_begin and rows_begin + n_rows <= Sk, n_rows >= 0; dk_rows
+ * and dv_rows 16-byte aligned and overlapping no other buffer. n_rows == 0 makes this
+ * fa_train_bwd_accum. Same workspace as fa_train_bwd_accum.
+ */
+FA_API fa_status fa_train_bwd_accum_rows(const fa_params* p, const void* q, const void* k, const void* v,
+                                         const void* mask, const void* o, const float* lse, const void* dO,
+                                         void* dq, float* dk_acc, float* dv_acc, int64_t rows_begin,
+                                         int32_t n_rows, void* dk_rows, void* dv_rows, void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/*
  * Tracing (optional). Kernels of the op, as named for fa_profile_set_events.
  * FA_KERNEL_FWD: the forward main kernel (plus the split-KV combine when used);
  * FA_KERNEL_BWD_MAIN: the backward main kernel(s) that form dQ/dK/dV;
@@ -184,10 +220,13 @@ FA_API fa_status fa_train_bwd_noalloc(const fa_params* p, const void* q, const v
 
 /*
  * Reads and clears the status word of the current device's kernels: 0 when
- * every wait inside a kernel completed; otherwise 0x80000000 | site, where site
- * names the wait that ran out of its time limit (the kernel then stopped early
- * and its outputs are invalid). Synchronous (waits for the device to finish the
- * copy). Returns FA_ERR_CUDA if no device is usable.
+ * every wait inside a kernel completed and no kernel found bad data; otherwise
+ * the first problem recorded since the last read: 0x80000000 | site when the wait
+ * `site` ran out of its time limit (the kernel then stopped early and its outputs
+ * are invalid), 0x40000000 | site when a kernel met a device-side argument it
+ * could not use (site 950: a row index of fa_set_rows_backward outside [0, S)).
+ * Synchronous (waits for the device to finish the copy). Returns FA_ERR_CUDA if
+ * no device is usable.
  */
 FA_API fa_status fa_device_status(uint32_t* out);
 

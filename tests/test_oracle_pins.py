@@ -352,3 +352,65 @@ def test_window_zero_width_band_is_the_diagonal():
         vis = [j for j in range(S) if abs(i - j) <= 1]
         np.testing.assert_allclose(o[0, 0, i], v[0, 0, vis].mean(0), atol=1e-14)
         np.testing.assert_allclose(lse[0, 0, i], math.log(len(vis)), atol=1e-14)
+
+
+# ---- SET_ROWS backward (the chunk's K/V gradient read back out of the window accumulator) ----
+
+from oracle import set_rows as rows_ref  # noqa: E402
+
+
+def test_set_rows_backward_is_the_autograd_of_a_row_write():
+    """torch autograd of index_copy (the row write of SET_ROWS) gives the source exactly the oracle's rows."""
+    rng = np.random.default_rng(31)
+    B, H, S, D = 2, 3, 11, 8
+    # the second index set repeats a row: each source row still receives the gradient at its row
+    for idx in (np.array([4, 9, 0, 7, 10]), np.array([4, 9, 4, 2])):
+        cache = torch.tensor(rng.standard_normal((B, H, S, D)))
+        src = torch.tensor(rng.standard_normal((B, H, len(idx), D)), requires_grad=True)
+        out = cache.index_copy(2, torch.tensor(idx), src)
+        g = torch.tensor(rng.standard_normal((B, H, S, D)))
+        (out * g).sum().backward()
+        np.testing.assert_array_equal(rows_ref.set_rows_backward(g.numpy(), idx), src.grad.numpy())
+
+
+def test_set_rows_backward_through_attention_on_the_cache():
+    """End to end: K/V written into a cache, attention over the cache; dL/d(written K/V) equals the
+    attention backward's dK/dV read back at the written rows (fp64 autograd vs oracle)."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 5, 12, 8
+    off = Sk - Sq
+    q = rng.standard_normal((B, Hq, Sq, D))
+    cache_k = rng.standard_normal((B, Hkv, Sk, D))
+    cache_v = rng.standard_normal((B, Hkv, Sk, D))
+    k_src = rng.standard_normal((B, Hkv, Sq, D))
+    v_src = rng.standard_normal((B, Hkv, Sq, D))
+    g = rng.standard_normal((B, Hq, Sq, D))
+    idx = np.arange(off, Sk)
+    tk = torch.tensor(k_src, requires_grad=True)
+    tv = torch.tensor(v_src, requires_grad=True)
+    kc = torch.tensor(cache_k).index_copy(2, torch.tensor(idx), tk)
+    vc = torch.tensor(cache_v).index_copy(2, torch.tensor(idx), tv)
+    G = Hq // Hkv
+    i = torch.arange(Sq)[:, None]
+    j = torch.arange(Sk)[None, :]
+    bias = torch.zeros(Sq, Sk, dtype=torch.float64).masked_fill(j > off + i, -math.inf)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q), kc.repeat_interleave(G, 1), vc.repeat_interleave(G, 1), attn_mask=bias, scale=0.3)
+    (o * torch.tensor(g)).sum().backward()
+    kk = cache_k.copy(); kk[:, :, idx] = k_src
+    vv = cache_v.copy(); vv[:, :, idx] = v_src
+    r = ref.backward(q, kk, vv, g, 0.3, causal=True, q_offset=off)
+    np.testing.assert_allclose(rows_ref.set_rows_backward(r["dk"], idx), tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rows_ref.set_rows_backward(r["dv"], idx), tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_bf16_rounding_matches_torch_including_ties():
+    rng = np.random.default_rng(33)
+    x = (rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)).astype(np.float32)
+    # exact ties: bf16 patterns with the dropped half equal to 0x8000, odd and even kept parts
+    base = rng.integers(0, 1 << 15, 512).astype(np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    ties_odd = ((base | 0x10000) | 0x8000).view(np.float32)
+    for v in (x, ties, ties_odd, np.array([0.0, -0.0, 1.0, -3.5, 1e-40], np.float32), x.reshape(4, 8, 128)):
+        want = torch.tensor(v).to(torch.bfloat16).float().numpy()
+        np.testing.assert_array_equal(rows_ref.to_bf16_bits(v), want)
