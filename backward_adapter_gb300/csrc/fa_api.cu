@@ -51,6 +51,10 @@ fa_status check_params(const fa_params* p, Shape& s) {
     set_error("mask_batch=%d must be 1 or B=%d", p->mask_batch, p->B); return FA_ERR_INVALID_ARG;
   }
   if (p->window < 0) { set_error("window=%d must be >= 0 (0 = no window)", p->window); return FA_ERR_INVALID_ARG; }
+  if (p->deterministic != 0 && p->deterministic != 1) {
+    set_error("deterministic=%d must be 0 or 1", p->deterministic); return FA_ERR_INVALID_ARG;
+  }
+  if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
   const bool positioned = p->causal || p->window > 0;
   if (positioned && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
     set_error("q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
@@ -64,6 +68,7 @@ fa_status check_params(const fa_params* p, Shape& s) {
   // nothing: drop it so no kernel pays for it
   s.window = (p->window > 0 && p->window < p->Sk) ? p->window : 0;
   s.q_offset = (p->causal || s.window > 0) ? (long long)p->q_offset : 0;
+  s.deterministic = p->deterministic;
   return FA_OK;
 }
 
@@ -190,8 +195,14 @@ BwdPlan plan_bwd(const Shape& s) {
   off = align_up(off + p.dsum_bytes);
   if (p.tensor_core) {
     p.dqacc_off = off;
-    p.dqacc_bytes = rows * s.D * 4;
+    p.dqacc_bytes = (size_t)dq_groups(s) * rows * s.D * 4;
     off = align_up(off + p.dqacc_bytes);
+    if (s.deterministic) {
+      // one turn counter per (key-tile group, batch, query head, 128-row query tile)
+      p.turn_off = off;
+      p.turn_bytes = (size_t)dq_groups(s) * s.B * s.Hq * ((s.Sq + 127) / 128) * 4;
+      off = align_up(off + p.turn_bytes);
+    }
   }
   p.total = off;
   return p;

@@ -50,7 +50,7 @@ __device__ __forceinline__ void store8(float* p, const float* x) {
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, const T* __restrict__ dO,
                                                    float* __restrict__ dsum, float* __restrict__ dq_acc,
-                                                   long long rows) {
+                                                   long long rows, int groups) {
   constexpr int LPR = D / 8;  // lanes per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = tid / LPR;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, cons
     for (int t = 0; t < 8; ++t) acc = fmaf(a[t], g[t], acc);
     if (dq_acc != nullptr) {
       const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      store8(dq_acc + row * D + part * 8, z);
+      for (int g = 0; g < groups; ++g) store8(dq_acc + ((long long)g * rows + row) * D + part * 8, z);
     }
   }
 #pragma unroll
@@ -74,11 +74,17 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, cons
 
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
-                                                         float scale, long long vecs) {
+                                                         float scale, long long vecs, int groups) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= vecs) return;
   float x[8];
   load8(acc + i * 8, x);
+  for (int g = 1; g < groups; ++g) {   // the key-tile groups' accumulators, always in group order
+    float y[8];
+    load8(acc + ((long long)g * vecs + i) * 8, y);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) x[t] += y[t];
+  }
 #pragma unroll
   for (int t = 0; t < 8; ++t) x[t] *= scale;
   store8(dq + i * 8, x);
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(256) mask_classify_kernel(Shape s, const void*
 
 }  // namespace
 
-cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero) {
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups) {
   const Shape& s = a.s;
   const long long rows = (long long)s.B * s.Hq * s.Sq;
   if (rows == 0) return cudaSuccess;
@@ -126,24 +132,24 @@ cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero) {
   if (s.dtype == DT_BF16) {
     if (s.D == 64)
       dsum_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups);
     else
       dsum_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups);
   } else {
     if (s.D == 64)
       dsum_kernel<float, 64><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                           dq_acc_to_zero, rows);
+                                                           dq_acc_to_zero, rows, groups);
     else
       dsum_kernel<float, 128><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                            dq_acc_to_zero, rows);
+                                                            dq_acc_to_zero, rows, groups);
   }
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_BWD_DSUM, a.stream);
 }
 
-cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc) {
+cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups) {
   const Shape& s = a.s;
   const long long vecs = (long long)s.B * s.Hq * s.Sq * s.D / 8;
   if (vecs == 0) return cudaSuccess;
@@ -151,9 +157,10 @@ cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc) {
   cudaError_t e = prof_begin(KID_BWD_DQCONV, a.stream);
   if (e != cudaSuccess) return e;
   if (s.dtype == DT_BF16)
-    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(dq_acc, (__nv_bfloat16*)a.dq, s.scale, vecs);
+    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(dq_acc, (__nv_bfloat16*)a.dq, s.scale, vecs,
+                                                                   groups);
   else
-    dq_convert_kernel<float><<<blocks, 256, 0, a.stream>>>(dq_acc, (float*)a.dq, s.scale, vecs);
+    dq_convert_kernel<float><<<blocks, 256, 0, a.stream>>>(dq_acc, (float*)a.dq, s.scale, vecs, groups);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_BWD_DQCONV, a.stream);

@@ -22,6 +22,7 @@ struct Shape {
   int mask_batch;
   int window;          // sliding-window half-width, 0 = none
   long long q_offset;  // key position of query row 0 (0 unless causal or windowed)
+  int deterministic;   // the backward adds dQ partials in a fixed order
 };
 
 struct FwdArgs {
@@ -71,7 +72,8 @@ struct BwdPlan {
   bool tensor_core;
   size_t tilemap_off, tilemap_bytes;
   size_t dsum_off, dsum_bytes;   // fp32 [B, Hq, Sq]
-  size_t dqacc_off, dqacc_bytes; // fp32 [B, Hq, Sq, D]
+  size_t dqacc_off, dqacc_bytes; // fp32 [groups, B, Hq, Sq, D]
+  size_t turn_off, turn_bytes;   // deterministic: int32 [groups, B, Hq, ceil(Sq / 128)] dQ turn counters
   size_t total;
 };
 
@@ -92,6 +94,12 @@ cudaError_t prof_begin(int kid, cudaStream_t st);
 cudaError_t prof_end(int kid, cudaStream_t st);
 void count_launches(int n);
 
+// Deterministic dQ: the key tiles form groups of kDetGroup consecutive 128-key tiles; each group
+// adds its partials in key-tile order into its own fp32 dQ accumulator, and the dQ convert pass
+// sums the groups' accumulators in group order. Without it there is one accumulator.
+constexpr int kDetGroup = 8;
+inline int dq_groups(const Shape& s) { return s.deterministic ? ((s.Sk + 127) / 128 + kDetGroup - 1) / kDetGroup : 1; }
+
 FwdPlan plan_fwd(const Shape& s);
 BwdPlan plan_bwd(const Shape& s);
 
@@ -100,8 +108,10 @@ cudaError_t simt_fwd(const FwdArgs& a);
 cudaError_t simt_bwd(const BwdArgs& a, float* dsum);
 
 // Helper passes shared by both paths.
-cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero);
-cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc);
+// dsum also zeroes `groups` fp32 dQ accumulators (none when dq_acc_to_zero is null); dq_convert
+// sums the groups in order, scales and converts to the dtype.
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups = 1);
+cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups = 1);
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
 
 // SET_ROWS backward gather (fa_set_rows_backward): out[bh, r, :] = acc[bh, idx[r], :].

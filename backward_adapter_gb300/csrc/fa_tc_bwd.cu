@@ -107,6 +107,7 @@ struct BwdTcParams {
   void* dk;  // bf16 [B,Hkv,Sk,D], or fp32 accumulator
   void* dv;
   int accum;
+  int* turn;              // deterministic: int32 [B, Hq, nqt] turn counters (zeroed before launch)
   long long rows_begin;   // accumulate: keys [rows_begin, rows_begin + n_rows) are also written, after
   int n_rows;             // the add, to dk_rows / dv_rows (bf16 [B, Hkv, n_rows, D])
   __nv_bfloat16* dk_rows;
@@ -116,18 +117,26 @@ struct BwdTcParams {
 };
 
 // The steps of a CTA: (query head of the group, query tile) pairs in a fixed order; the tiles
-// run over the rows [ibeg, iend) that can see the CTA's keys.
+// run over the rows [ibeg, iend) that can see the CTA's keys. Head-major with ascending tiles by
+// default; with tile_major (deterministic dQ) descending tiles with every head of the group at
+// each tile, so that all key tiles reach a given query tile at about the same step.
 struct StepIter {
-  int G, iend, BQ, ibeg;
+  int G, iend, BQ, ibeg, last;
+  bool tile_major;
   int hh, i0;
-  __device__ void init(int G_, int iend_, int BQ_, int ibeg_) {
-    G = G_; iend = iend_; BQ = BQ_; ibeg = ibeg_;
-    hh = 0; i0 = ibeg;
+  __device__ void init(int G_, int iend_, int BQ_, int ibeg_, bool tile_major_) {
+    G = G_; iend = iend_; BQ = BQ_; ibeg = ibeg_; tile_major = tile_major_;
+    last = ibeg < iend ? ibeg + ((iend - 1 - ibeg) / BQ) * BQ : ibeg;
+    hh = 0; i0 = tile_major ? last : ibeg;
   }
-  __device__ bool valid() const { return hh < G && ibeg < iend; }
+  __device__ bool valid() const { return ibeg < iend && (tile_major ? i0 >= ibeg : hh < G); }
   __device__ void next() {
-    i0 += BQ;
-    if (i0 >= iend) { i0 = ibeg; ++hh; }
+    if (tile_major) {
+      if (++hh == G) { hh = 0; i0 -= BQ; }
+    } else {
+      i0 += BQ;
+      if (i0 >= iend) { i0 = ibeg; ++hh; }
+    }
   }
 };
 
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       }
       uint32_t used_mask = 0, phase_mask = 0;
       StepIter it;
-      it.init(G, iend, BQ, ibeg);
+      it.init(G, iend, BQ, ibeg, s.deterministic != 0);
       for (int st = 0; it.valid(); it.next()) {
         if (step_skipped(it)) continue;
         const int slot = st % C::NSTAGE;
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       int total = 0;
       {
         StepIter it;
-        it.init(G, iend, BQ, ibeg);
+        it.init(G, iend, BQ, ibeg, s.deterministic != 0);
         for (; it.valid(); it.next())
           if (!step_skipped(it)) ++total;
       }
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else if (warp == 2) {
     // ---------------------------------------------------------------- LSE / D staging
     StepIter it;
-    it.init(G, iend, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
     const float l2e = kLog2e;
     for (int st = 0; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
@@ -428,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
 
     StepIter it;
-    it.init(G, iend, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
     int st = 0;
     bool ok = true;
     for (; it.valid(); it.next()) {
@@ -617,10 +626,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
     StepIter it;
-    it.init(G, iend, BQ, ibeg);
+    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    // Deterministic dQ: the key tiles form groups of kDetGroup; each group has its own fp32 dQ
+    // accumulator (summed in group order by the convert pass), and within a group the key tiles that
+    // see a query tile add their partials to it in ascending key-tile order. A turn counter per
+    // (group, batch, query head, query tile) counts the passes: every stager warp (D = 128) or the
+    // leader thread (D = 64) of each earlier key tile adds one once its partial is added, steps the
+    // tile map skips included. The key tiles that see query tile i0 are the consecutive tiles from
+    // kt_first(i0) on, so a tile's rank in its group follows from the shape alone.
+    constexpr int kPassesPerCta = C::RED_DQ ? 4 : 1;
+    const int group = s.deterministic ? kt / kDetGroup : 0;
+    const size_t bhq = (size_t)s.B * s.Hq;
+    float* dq_acc_g = p.dq_acc + (size_t)group * bhq * s.Sq * D;
+    auto turn_of = [&](const StepIter& t) -> int* {
+      return p.turn + ((size_t)group * bhq + (size_t)(b * s.Hq + kvh * G + t.hh)) * p.nqt + t.i0 / 128;
+    };
+    auto rank_of = [&](const StepIter& t) -> int {
+      const long long kt_first = s.window > 0 ? max(0LL, s.q_offset + t.i0 - s.window) / kBN : 0;
+      return kt - (int)max(kt_first, (long long)group * kDetGroup);
+    };
     int st = 0;
     for (; it.valid(); it.next()) {
-      if (step_skipped(it)) continue;
+      if (step_skipped(it)) {
+        if (!s.deterministic) continue;
+        // no partial from this key tile here, but its turn still passes
+        int* turn = turn_of(it);
+        const bool mine = C::RED_DQ ? lane == 0 : leader;
+        bool ok2 = true;
+        if (mine) {
+          ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 140);
+          if (ok2) red_release_gpu_add(turn, 1);
+        }
+        if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
+        continue;
+      }
       const int slot = st % C::NSTAGE, buf = st % C::NBUF;
       float* sdq = reinterpret_cast<float*>(smem + C::OFF_STAGE + slot * 2 * C::Q_TILE);
       const uint32_t sbase = smem_u32(sdq);
@@ -643,12 +682,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // run of 32 consecutive features of one query row (rows past Sq are not touched)
         const int d = wq * 32 + lane;
         const int nrows = min(BQ, s.Sq - it.i0);
-        float* dst = p.dq_acc + ((size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq + it.i0) * D + d;
+        float* dst = dq_acc_g + ((size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq + it.i0) * D + d;
+        int* turn = s.deterministic ? turn_of(it) : nullptr;
+        if (turn != nullptr) {
+          // this warp adds once the earlier key tiles of its group have passed (acquire by lane 0,
+          // then the whole warp)
+          bool ok2 = true;
+          if (lane == 0) ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 141);
+          if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
+          __syncwarp();
+          fence_acq_rel_gpu();
+        }
 #pragma unroll
         for (int c = 0; c < C::DQ_CHUNKS; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e < nrows) red_add_f32(dst + (size_t)(c * 32 + e) * D, __uint_as_float(v[c][e]));
+        }
+        if (turn != nullptr) {
+          // every lane's adds are performed before lane 0 passes the turn (release)
+          fence_acq_rel_gpu();
+          __syncwarp();
+          if (lane == 0) red_release_gpu_add(turn, 1);
         }
       } else {
         // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read:
@@ -672,12 +727,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         bool filled = true;
         if (leader) filled = mbar_wait(bar_stage_full, st & 1, abort_flag, p.status, 136);
         if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
+        bool ok2 = true;
         if (leader) {
-          tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, b * s.Hq + kvh * G + it.hh);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bar_qdo_empty[slot]);
+          int* turn = s.deterministic ? turn_of(it) : nullptr;
+          if (turn != nullptr) {
+            ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 142);
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+          }
+          if (ok2) {
+            tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, (int)(group * bhq) + b * s.Hq + kvh * G + it.hh);
+            bulk_commit_group();
+            if (turn != nullptr) {
+              // the whole add is complete and visible before the turn passes
+              bulk_wait_group0();
+              fence_proxy_async_global();
+              fence_acq_rel_gpu();
+              red_release_gpu_add(turn, 1);
+            } else {
+              bulk_wait_group_read0();
+            }
+            mbar_arrive(&bar_qdo_empty[slot]);
+          }
         }
+        if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
       }
       ++st;
     }
@@ -707,7 +780,8 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
   if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
   float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
-  if ((e = make_tmap_f32_bhsd(&p.tm_dq, dq_acc, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
+  const int groups = dq_groups(s);
+  if ((e = make_tmap_f32_bhsd(&p.tm_dq, dq_acc, s.Sq, groups * s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + 127) / 128;
@@ -719,7 +793,7 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.tilemap = tm;
   }
   float* dsum = reinterpret_cast<float*>(ws + plan.dsum_off);
-  if ((e = launch_dsum(a, dsum, dq_acc)) != cudaSuccess) return e;
+  if ((e = launch_dsum(a, dsum, dq_acc, groups)) != cudaSuccess) return e;
   p.lse = a.lse;
   p.dsum = dsum;
   p.dq_acc = dq_acc;
@@ -731,6 +805,11 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   p.dk_rows = static_cast<__nv_bfloat16*>(a.dk_rows);
   p.dv_rows = static_cast<__nv_bfloat16*>(a.dv_rows);
   p.status = status;
+  p.turn = nullptr;
+  if (s.deterministic) {
+    p.turn = reinterpret_cast<int*>(ws + plan.turn_off);
+    if ((e = cudaMemsetAsync(p.turn, 0, plan.turn_bytes, a.stream)) != cudaSuccess) return e;
+  }
   const int smem = C::BYTES;
   if ((e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
@@ -741,7 +820,7 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = prof_end(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
-  return launch_dq_convert(a, dq_acc);
+  return launch_dq_convert(a, dq_acc, groups);
 }
 
 cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws) {

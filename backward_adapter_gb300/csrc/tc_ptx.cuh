@@ -130,6 +130,37 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Acquire load / release add of a global int at GPU scope (turn counters between CTAs).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Wait (bounded, like mbar_wait) until *p >= target; records `site` and sets *abort on timeout.
+__device__ __forceinline__ bool wait_turn(const int* p, int target, volatile int* abort, unsigned* status,
+                                          unsigned site, unsigned long long limit_ns = kWaitLimitNs) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        if (abort != nullptr) *abort = 1;
+        atomicCAS(status, 0u, 0x80000000u | site);
+        return false;
+      }
+    }
+  }
+}
+
 // Fire-and-forget fp32 add into global memory (performed in L2).
 __device__ __forceinline__ void red_add_f32(float* ptr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");

@@ -33,7 +33,7 @@ class FaParams(ctypes.Structure):
                 ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("mask_kind", ctypes.c_int32), ("mask_batch", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("q_offset", ctypes.c_int64)]
+                ("q_offset", ctypes.c_int64), ("deterministic", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class FaError(RuntimeError):
@@ -128,11 +128,12 @@ def _mask_view(mask: Optional[torch.Tensor]):
 
 def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] = None, *,
                 scale: Optional[float] = None, causal: bool = False,
-                q_offset: Optional[int] = None, window: int = 0) -> FaParams:
+                q_offset: Optional[int] = None, window: int = 0, deterministic: bool = False) -> FaParams:
     """Fill fa_params from tensor shapes. q: [B,Hq,Sq,D], k: [B,Hkv,Sk,D].
 
     q_offset (causal or windowed) defaults to Sk - Sq: the query rows are the last Sq
-    key positions. window is the sliding-window half-width (0 = none).
+    key positions. window is the sliding-window half-width (0 = none). deterministic makes
+    the backward's dQ bitwise reproducible.
     """
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
@@ -142,7 +143,7 @@ def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] =
     if q_offset is None:
         q_offset = Sk - Sq if (causal or window > 0) else 0
     return FaParams(B, Hq, Hkv, Sq, Sk, D, _dtype_code(q), float(scale), int(bool(causal)), kind, mb,
-                    int(window), int(q_offset))
+                    int(window), int(q_offset), int(bool(deterministic)), 0)
 
 
 def fwd_workspace_size(p: FaParams) -> int:
@@ -173,13 +174,14 @@ def _need_cuda(*ts):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
 
 
-def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, out=None, lse=None,
+def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, out=None, lse=None,
         workspace=None, stream=None):
     """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, mview)
-    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -191,13 +193,14 @@ def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0
     return out, lse
 
 
-def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, dq=None, dk=None,
+def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk=None,
         dv=None, workspace=None, stream=None):
     """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
-    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -209,7 +212,7 @@ def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=No
     return dq, dk, dv
 
 
-def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, causal=False, q_offset=None, window=0,
+def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False,
               dq=None, workspace=None, stream=None):
     """Accumulating backward: dK/dV are added into fp32 dk_acc/dv_acc in place; returns dQ."""
     lib = load_library()
@@ -217,7 +220,8 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
     _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
-    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
@@ -228,7 +232,7 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
 
 
 def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows: int, mask=None, *, scale=None,
-                   causal=False, q_offset=None, window=0, dq=None, dk_rows=None, dv_rows=None, workspace=None,
+                   causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk_rows=None, dv_rows=None, workspace=None,
                    stream=None):
     """Accumulating backward fused with the SET_ROWS backward of keys [rows_begin, rows_begin + n_rows).
 
@@ -240,7 +244,8 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
     _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
-    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     shape = (k.shape[0], k.shape[1], int(n_rows), k.shape[3])
     dk_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dk_rows is None else dk_rows
@@ -300,7 +305,7 @@ def device_status() -> int:
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
-def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, dq=None, dk=None,
+def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk=None,
                 dv=None, stream=None):
     """Backward through fa_train_bwd_noalloc: no workspace is allocated or passed.
 
@@ -312,7 +317,8 @@ def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_o
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
-    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window)
+    p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

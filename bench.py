@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="bitwise reproducible dQ (partials added in a fixed key-tile order)")
     return ap.parse_args(argv)
 
 
@@ -254,7 +256,7 @@ def run_ours(args):
         host["mask"] = torch.from_numpy(inputs["mask"]).pin_memory()
     d = {n: t.to(dev) for n, t in host.items()}
     mask = d.get("mask")
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=args.deterministic)
     p = ft.make_params(d["q"], d["k"], mask, **kw)
     ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
@@ -428,6 +430,7 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask, "accum": w.accum,
                    "rows_read_back": [w.q_offset, w.Sq] if w.accum else None,
+                   "deterministic": bool(args.deterministic),
                    "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
                    "l2": "flushed (256 MiB write) between timed steps, outside the step events",
                    "parallelism": f"replicas x{world}"},

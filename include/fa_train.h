@@ -98,6 +98,10 @@ typedef struct fa_params {
   int32_t window;     /* sliding-window half-width w >= 0; 0 = no window */
   int64_t q_offset;   /* causal or window > 0: key position of query row 0; needs 0 <= q_offset and
                          q_offset + Sq <= Sk. Ignored (taken as 0) when neither is set. */
+  int32_t deterministic; /* 0 or 1. 1: the backward's dQ is bitwise reproducible from run to run
+                            (its per-key-tile partials are added in a fixed order); dK/dV always are.
+                            Costs some backward speed and a few bytes of workspace. */
+  int32_t reserved;   /* must be 0 */
 } fa_params;
 
 /* Bytes of scratch the forward needs for these parameters (0 when none). */

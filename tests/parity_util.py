@@ -29,9 +29,9 @@ def to_device(inputs: dict, w: wl.Workload, device="cuda"):
     return t
 
 
-def run_gpu(w: wl.Workload, t: dict) -> dict:
+def run_gpu(w: wl.Workload, t: dict, deterministic: bool = False) -> dict:
     """Forward + backward on the GPU; returns float64 numpy copies of every output."""
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=deterministic)
     o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
     if w.accum:
         dk, dv = t["dk_acc"].clone(), t["dv_acc"].clone()

@@ -92,6 +92,31 @@ def test_dirty_pad_is_bitwise_invisible():
         assert np.array_equal(a["dv"][b, :, :lens[b]], bb["dv"][b, :, :lens[b]])
 
 
+DETERMINISTIC = [
+    W("det_causal_gqa_d128", B=1, Hq=8, Hkv=2, Sq=640, Sk=640, D=128, causal=True, seed=71),
+    W("det_cross_skip_tiles_d128", B=2, Hq=2, Hkv=2, Sq=300, Sk=520, D=128, mask="cross", seed=72),
+    W("det_window_pad_d64", B=1, Hq=4, Hkv=2, Sq=700, Sk=700, D=64, window=100, mask="pad_self", seed=73),
+    W("det_causal_offset_accum_d64", B=1, Hq=4, Hkv=1, Sq=200, Sk=900, D=64, causal=True, q_offset=700,
+      accum=True, seed=74),
+    W("det_window_chunk_mid_d128", B=1, Hq=2, Hkv=1, Sq=300, Sk=1000, D=128, q_offset=200, window=150, seed=75),
+]
+
+
+@pytest.mark.parametrize("w", DETERMINISTIC, ids=[w.name for w in DETERMINISTIC])
+def test_deterministic_dq_is_bitwise_reproducible_and_matches_oracle(w):
+    """With deterministic set, dQ (whose partials come from many key tiles) is bitwise identical
+    from run to run, including tiles the mask skips; every output still matches the oracle."""
+    inputs = wl.make_inputs(w)
+    t = pu.to_device(inputs, w)
+    runs = [pu.run_gpu(w, t, deterministic=True) for _ in range(3)]
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        for r in runs[1:]:
+            assert np.array_equal(runs[0][n], r[n]), n
+    exp = pu.run_oracle(w, inputs)
+    pu.assert_parity(w, runs[0], exp)
+    pu.assert_exact_zeros(w, inputs, runs[0])
+
+
 def test_dk_dv_are_deterministic():
     w = W("bf16_determinism", B=1, Hq=8, Hkv=2, Sq=512, Sk=512, D=128, causal=True, seed=27)
     t = pu.to_device(wl.make_inputs(w), w)
