@@ -54,7 +54,9 @@ fa_status check_params(const fa_params* p, Shape& s) {
   if (p->deterministic != 0 && p->deterministic != 1) {
     set_error("deterministic=%d must be 0 or 1", p->deterministic); return FA_ERR_INVALID_ARG;
   }
-  if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
+  if (p->kv_format != FA_KV_DTYPE && p->kv_format != FA_KV_Q8_0) {
+    set_error("kv_format=%d invalid", p->kv_format); return FA_ERR_INVALID_ARG;
+  }
   const bool positioned = p->causal || p->window > 0;
   if (positioned && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
     set_error("q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
@@ -69,6 +71,7 @@ fa_status check_params(const fa_params* p, Shape& s) {
   s.window = (p->window > 0 && p->window < p->Sk) ? p->window : 0;
   s.q_offset = (p->causal || s.window > 0) ? (long long)p->q_offset : 0;
   s.deterministic = p->deterministic;
+  s.kv_q8 = p->kv_format == FA_KV_Q8_0 ? 1 : 0;
   return FA_OK;
 }
 
@@ -167,6 +170,12 @@ FwdPlan plan_fwd(const Shape& s) {
     p.tilemap_bytes = (size_t)s.mask_batch * ((s.Sq + 127) / 128) * ((s.Sk + 127) / 128);
     off = align_up(off + p.tilemap_bytes);
   }
+  if (p.tensor_core && s.kv_q8) {
+    // the q8_0 cache dequantized to bf16 K then V (read by every query tile of the forward)
+    p.kvbf_off = off;
+    p.kvbf_bytes = 2 * (size_t)s.B * s.Hkv * s.Sk * s.D * 2;
+    off = align_up(off + p.kvbf_bytes);
+  }
   if (p.kv_splits > 1) {
     const size_t rows = (size_t)s.B * s.Hq * s.Sq;
     p.part_o_off = off;
@@ -226,24 +235,80 @@ size_t fa_train_bwd_workspace_size(const fa_params* p) {
   return plan_bwd(s).total;
 }
 
-fa_status fa_train_fwd(const fa_params* p, const void* q, const void* k, const void* v, const void* mask, void* o,
-                       float* lse, void* ws, size_t ws_bytes, void* stream) {
+// The K/V inputs of a call: tensors in the params' dtype, or a q8_0 cache (value and scale planes).
+struct KvIn {
+  const void* k;
+  const void* v;
+  const fa_kv_q8* q8;
+};
+
+// Appends the K/V input spans to `in` (2 for tensors, 4 for a q8_0 cache).
+static fa_status kv_spans(const Shape& s, const KvIn& kv, Span* in, int& n) {
+  if ((kv.q8 != nullptr) != (s.kv_q8 != 0)) {
+    set_error(s.kv_q8 ? "kv_format is FA_KV_Q8_0: use the _q8 entry points" : "the _q8 entry points need kv_format FA_KV_Q8_0");
+    return FA_ERR_INVALID_ARG;
+  }
+  if (kv.q8 == nullptr) {
+    const size_t es = elem_size(s);
+    in[n++] = {kv.k, kv_bytes(s, es), "k"};
+    in[n++] = {kv.v, kv_bytes(s, es), "v"};
+    return FA_OK;
+  }
+  if (s.dtype != DT_BF16) { set_error("a q8_0 K/V cache needs bf16 queries (dtype=%d)", s.dtype); return FA_ERR_UNSUPPORTED; }
+  const size_t scales = (size_t)s.B * s.Hkv * s.Sk * (s.D / 32) * 2;
+  in[n++] = {kv.q8->k_q, kv_bytes(s, 1), "k_q"};
+  in[n++] = {kv.q8->k_d, scales, "k_d"};
+  in[n++] = {kv.q8->v_q, kv_bytes(s, 1), "v_q"};
+  in[n++] = {kv.q8->v_d, scales, "v_d"};
+  return FA_OK;
+}
+
+static fa_status fwd_common(const fa_params* p, const void* q, const KvIn& kv, const void* mask, void* o, float* lse,
+                            void* ws, size_t ws_bytes, void* stream) {
   Shape s;
   fa_status st = check_params(p, s);
   if (st != FA_OK) return st;
-  const size_t es = elem_size(s);
-  const Span in[] = {{q, q_bytes(s), "q"}, {k, kv_bytes(s, es), "k"}, {v, kv_bytes(s, es), "v"},
-                     {mask, mask_bytes(s), "mask"}};
+  Span in[7];
+  int nin = 0;
+  in[nin++] = {q, q_bytes(s), "q"};
+  if ((st = kv_spans(s, kv, in, nin)) != FA_OK) return st;
+  in[nin++] = {mask, mask_bytes(s), "mask"};
   const Span out[] = {{o, q_bytes(s), "o"}, {lse, (size_t)s.B * s.Hq * s.Sq * 4, "lse"}};
-  if ((st = check_buffers(in, 4, out, 2)) != FA_OK) return st;
+  if ((st = check_buffers(in, nin, out, 2)) != FA_OK) return st;
   const FwdPlan plan = plan_fwd(s);
-  const Span all[] = {in[0], in[1], in[2], in[3], out[0], out[1]};
-  if ((st = check_ws(ws, ws_bytes, plan.total, all, 6)) != FA_OK) return st;
+  Span all[9];
+  for (int i = 0; i < nin; ++i) all[i] = in[i];
+  all[nin] = out[0];
+  all[nin + 1] = out[1];
+  if ((st = check_ws(ws, ws_bytes, plan.total, all, nin + 2)) != FA_OK) return st;
   if (s.Sq == 0) return FA_OK;
+  if (kv.q8 != nullptr && !plan.tensor_core) { set_error("a q8_0 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED; }
 
-  FwdArgs a{s, q, k, v, mask, o, lse, (cudaStream_t)stream};
-  cudaError_t e = plan.tensor_core ? tc_fwd(a, plan, (char*)ws) : simt_fwd(a);
+  FwdArgs a{s, q, kv.k, kv.v, mask, o, lse, (cudaStream_t)stream};
+  cudaError_t e = cudaSuccess;
+  if (kv.q8 != nullptr) {
+    // every query tile reads every key tile: dequantize the cache once, then run the bf16 kernel on it
+    char* kbf = (char*)ws + plan.kvbf_off;
+    char* vbf = kbf + plan.kvbf_bytes / 2;
+    e = launch_q8_dequant(s, kv.q8->k_q, kv.q8->k_d, kbf, a.stream);
+    if (e == cudaSuccess) e = launch_q8_dequant(s, kv.q8->v_q, kv.q8->v_d, vbf, a.stream);
+    if (e != cudaSuccess) return cuda_status(e, "q8_0 dequantize launch");
+    a.k = kbf;
+    a.v = vbf;
+  }
+  e = plan.tensor_core ? tc_fwd(a, plan, (char*)ws) : simt_fwd(a);
   return cuda_status(e, "forward launch");
+}
+
+fa_status fa_train_fwd(const fa_params* p, const void* q, const void* k, const void* v, const void* mask, void* o,
+                       float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return fwd_common(p, q, KvIn{k, v, nullptr}, mask, o, lse, ws, ws_bytes, stream);
+}
+
+fa_status fa_train_fwd_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask, void* o,
+                          float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (kv == nullptr) { g_last_error[0] = '\0'; set_error("kv is NULL"); return FA_ERR_INVALID_ARG; }
+  return fwd_common(p, q, KvIn{nullptr, nullptr, kv}, mask, o, lse, ws, ws_bytes, stream);
 }
 
 // Rows of the accumulator written back out by the fused SET_ROWS backward (n_rows == 0: none).
@@ -254,7 +319,7 @@ struct RowsOut {
   void* dv = nullptr;
 };
 
-static fa_status bwd_common(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
+static fa_status bwd_common(const fa_params* p, const void* q, const KvIn& kv, const void* mask,
                             const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             bool accum, void* ws, size_t ws_bytes, void* stream, const RowsOut& rb = RowsOut{}) {
   Shape s;
@@ -262,9 +327,14 @@ static fa_status bwd_common(const fa_params* p, const void* q, const void* k, co
   if (st != FA_OK) return st;
   const size_t es = elem_size(s);
   const size_t rows = (size_t)s.B * s.Hq * s.Sq;
-  const Span in[] = {{q, q_bytes(s), "q"}, {k, kv_bytes(s, es), "k"}, {v, kv_bytes(s, es), "v"},
-                     {mask, mask_bytes(s), "mask"}, {o, q_bytes(s), "o"}, {lse, rows * 4, "lse"},
-                     {dO, q_bytes(s), "dO"}};
+  Span in[10];
+  int nin = 0;
+  in[nin++] = {q, q_bytes(s), "q"};
+  if ((st = kv_spans(s, kv, in, nin)) != FA_OK) return st;
+  in[nin++] = {mask, mask_bytes(s), "mask"};
+  in[nin++] = {o, q_bytes(s), "o"};
+  in[nin++] = {lse, rows * 4, "lse"};
+  in[nin++] = {dO, q_bytes(s), "dO"};
   const size_t gk = accum ? kv_bytes(s, 4) : kv_bytes(s, es);
   if (rb.n < 0 || rb.begin < 0 || rb.begin + rb.n > s.Sk) {
     set_error("rows [%lld, %lld) outside the %d keys", rb.begin, rb.begin + rb.n, s.Sk);
@@ -274,10 +344,12 @@ static fa_status bwd_common(const fa_params* p, const void* q, const void* k, co
   const Span out[] = {{dq, q_bytes(s), "dq"}, {dk, gk, accum ? "dk_acc" : "dk"}, {dv, gk, accum ? "dv_acc" : "dv"},
                       {rb.dk, gr, "dk_rows"}, {rb.dv, gr, "dv_rows"}};
   const int n_out = rb.n > 0 ? 5 : 3;
-  if ((st = check_buffers(in, 7, out, n_out)) != FA_OK) return st;
+  if ((st = check_buffers(in, nin, out, n_out)) != FA_OK) return st;
   const BwdPlan plan = plan_bwd(s);
-  const Span all[] = {in[0], in[1], in[2], in[3], in[4], in[5], in[6], out[0], out[1], out[2], out[3], out[4]};
-  if ((st = check_ws(ws, ws_bytes, plan.total, all, 7 + n_out)) != FA_OK) return st;
+  Span all[15];
+  for (int i = 0; i < nin; ++i) all[i] = in[i];
+  for (int i = 0; i < n_out; ++i) all[nin + i] = out[i];
+  if ((st = check_ws(ws, ws_bytes, plan.total, all, nin + n_out)) != FA_OK) return st;
 
   cudaStream_t cs = (cudaStream_t)stream;
   if (s.Sq == 0) {
@@ -293,7 +365,14 @@ static fa_status bwd_common(const fa_params* p, const void* q, const void* k, co
     if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, gk, cs);
     return cuda_status(e, "zero dK/dV");
   }
-  BwdArgs a{s, q, k, v, mask, o, lse, dO, dq, dk, dv, accum, cs};
+  if (kv.q8 != nullptr && !plan.tensor_core) { set_error("a q8_0 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED; }
+  BwdArgs a{s, q, kv.k, kv.v, mask, o, lse, dO, dq, dk, dv, accum, cs};
+  if (kv.q8 != nullptr) {
+    a.kq = kv.q8->k_q;
+    a.kd = kv.q8->k_d;
+    a.vq = kv.q8->v_q;
+    a.vd = kv.q8->v_d;
+  }
   a.rows_begin = rb.begin;
   a.n_rows = rb.n;
   a.dk_rows = rb.dk;
@@ -306,13 +385,28 @@ static fa_status bwd_common(const fa_params* p, const void* q, const void* k, co
 fa_status fa_train_bwd(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
                        const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv, void* ws,
                        size_t ws_bytes, void* stream) {
-  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk, dv, false, ws, ws_bytes, stream);
+  return bwd_common(p, q, KvIn{k, v, nullptr}, mask, o, lse, dO, dq, dk, dv, false, ws, ws_bytes, stream);
 }
 
 fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
                              const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
                              float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
-  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream);
+  return bwd_common(p, q, KvIn{k, v, nullptr}, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream);
+}
+
+fa_status fa_train_bwd_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                          void* stream) {
+  if (kv == nullptr) { g_last_error[0] = '\0'; set_error("kv is NULL"); return FA_ERR_INVALID_ARG; }
+  return bwd_common(p, q, KvIn{nullptr, nullptr, kv}, mask, o, lse, dO, dq, dk, dv, false, ws, ws_bytes, stream);
+}
+
+fa_status fa_train_bwd_accum_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask,
+                                const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
+                                float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
+  if (kv == nullptr) { g_last_error[0] = '\0'; set_error("kv is NULL"); return FA_ERR_INVALID_ARG; }
+  return bwd_common(p, q, KvIn{nullptr, nullptr, kv}, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes,
+                    stream);
 }
 
 fa_status fa_train_bwd_accum_rows(const fa_params* p, const void* q, const void* k, const void* v, const void* mask,
@@ -324,7 +418,8 @@ fa_status fa_train_bwd_accum_rows(const fa_params* p, const void* q, const void*
   rows.n = n_rows;
   rows.dk = dk_rows;
   rows.dv = dv_rows;
-  return bwd_common(p, q, k, v, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream, rows);
+  return bwd_common(p, q, KvIn{k, v, nullptr}, mask, o, lse, dO, dq, dk_acc, dv_acc, true, ws, ws_bytes, stream,
+                    rows);
 }
 
 fa_status fa_set_rows_backward(const float* acc, int32_t B, int32_t H, int32_t S, int32_t D, const int64_t* idx,

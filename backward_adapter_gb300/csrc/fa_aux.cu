@@ -9,10 +9,12 @@
 // Each thread moves 16-byte vectors; rows are split across 8..16 lanes. The file also holds
 // the self-test of the kernels' bounded waits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
+#include "kv_q8.cuh"
 #include "tc_ptx.cuh"
 
 namespace fa {
@@ -205,6 +207,43 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
   unsigned* status = device_status_ptr();
   if (status == nullptr) return cudaErrorUnknown;
   wait_selftest_kernel<<<1, 1, 0, st>>>(status, limit_ns);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+namespace fa {
+namespace {
+
+// One thread per 16 features of a key row: one 16-byte load of values, one scale, 32 bytes out.
+__global__ void __launch_bounds__(256) q8_dequant_kernel(const int8_t* __restrict__ xq, const __half* __restrict__ xd,
+                                                         __nv_bfloat16* __restrict__ out, long long segs) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= segs) return;
+  const long long e0 = i * 16;           // first feature of the segment; its scale is e0 / 32
+  const int4 raw = __ldg(reinterpret_cast<const int4*>(xq + e0));
+  const float scale = __half2float(xd[e0 / 32]);
+  const uint32_t uw[4] = {(uint32_t)raw.x ^ 0x80808080u, (uint32_t)raw.y ^ 0x80808080u,
+                          (uint32_t)raw.z ^ 0x80808080u, (uint32_t)raw.w ^ 0x80808080u};
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = tc::pack_bf16x2(s8_to_f32(uw[k / 2], (k % 2) * 2) * scale, s8_to_f32(uw[k / 2], (k % 2) * 2 + 1) * scale);
+  uint4* dst = reinterpret_cast<uint4*>(out + e0);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+}  // namespace
+
+cudaError_t launch_q8_dequant(const Shape& s, const int8_t* xq, const void* xd, void* out, cudaStream_t st) {
+  const long long segs = (long long)s.B * s.Hkv * s.Sk * s.D / 16;
+  if (segs == 0) return cudaSuccess;
+  const long long blocks = (segs + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  q8_dequant_kernel<<<(unsigned)blocks, 256, 0, st>>>(xq, static_cast<const __half*>(xd),
+                                                       static_cast<__nv_bfloat16*>(out), segs);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -23,6 +23,7 @@ struct Shape {
   int window;          // sliding-window half-width, 0 = none
   long long q_offset;  // key position of query row 0 (0 unless causal or windowed)
   int deterministic;   // the backward adds dQ partials in a fixed order
+  int kv_q8;           // K/V come from a q8_0 cache
 };
 
 struct FwdArgs {
@@ -56,6 +57,11 @@ struct BwdArgs {
   int n_rows = 0;
   void* dk_rows = nullptr;
   void* dv_rows = nullptr;
+  // q8_0 K/V cache (k, v unused when kq != nullptr): int8 [B, Hkv, Sk, D] + fp16 [B, Hkv, Sk, D / 32]
+  const int8_t* kq = nullptr;
+  const void* kd = nullptr;
+  const int8_t* vq = nullptr;
+  const void* vd = nullptr;
 };
 
 // Carve-up of the caller's workspace. Offsets are 256-byte aligned.
@@ -65,6 +71,7 @@ struct FwdPlan {
   size_t tilemap_off, tilemap_bytes;
   size_t part_o_off, part_o_bytes;     // fp32 [splits, B, Hq, Sq, D]
   size_t part_ml_off, part_ml_bytes;   // fp32 [splits, B, Hq, Sq, 2]
+  size_t kvbf_off, kvbf_bytes;         // q8_0 cache: bf16 K then V [B, Hkv, Sk, D]
   size_t total;
 };
 
@@ -113,6 +120,9 @@ cudaError_t simt_bwd(const BwdArgs& a, float* dsum);
 cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups = 1);
 cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups = 1);
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
+
+// q8_0 cache -> bf16 [B, Hkv, Sk, D] (x = scale[d / 32] * q[d], rounded to nearest even).
+cudaError_t launch_q8_dequant(const Shape& s, const int8_t* xq, const void* xd, void* out, cudaStream_t st);
 
 // SET_ROWS backward gather (fa_set_rows_backward): out[bh, r, :] = acc[bh, idx[r], :].
 constexpr unsigned kSiteRowIndex = 950;

@@ -33,11 +33,14 @@
 // dV / dK have read it. D = 64: the dQ partial is staged in the step's consumed Q/dO
 // slot and added with one TMA bulk tensor reduce-add.
 #include <cuda.h>
+#include <cstring>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
+#include "kv_q8.cuh"
 #include "tc_ptx.cuh"
 
 namespace fa {
@@ -108,6 +111,11 @@ struct BwdTcParams {
   void* dv;
   int accum;
   int* turn;              // deterministic: int32 [B, Hq, nqt] turn counters (zeroed before launch)
+  int q8;                 // q8_0 K/V cache: the softmax-grad warps dequantize the CTA's K, V tiles
+  const int8_t* kq;
+  const __half* kd;
+  const int8_t* vq;
+  const __half* vd;
   long long rows_begin;   // accumulate: keys [rows_begin, rows_begin + n_rows) are also written, after
   int n_rows;             // the add, to dk_rows / dv_rows (bf16 [B, Hkv, n_rows, D])
   __nv_bfloat16* dk_rows;
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int iend = (int)max((long long)ibeg, last + 1);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_kv, p.q8 ? 8 : 1);   // q8: one arrival per softmax-grad warp after dequantizing
     for (int i = 0; i < C::NSTAGE; ++i) {
       mbar_init(&bar_qdo_full[i], 1);
       mbar_init(&bar_qdo_empty[i], 1);
@@ -232,15 +240,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
-      prefetch_tmap(&p.tm_k);
-      prefetch_tmap(&p.tm_v);
       prefetch_tmap(&p.tm_do);
-      prefetch_tmap(&p.tm_dq);
+      if (!C::RED_DQ) prefetch_tmap(&p.tm_dq);
       const int kvrow = b * s.Hkv + kvh;
-      mbar_arrive_expect_tx(bar_kv, 2 * C::KV_TILE);
-      for (int box = 0; box < D / 64; ++box) {
-        tma_load_3d(smem + C::OFF_K + box * C::KV_BOX, &p.tm_k, bar_kv, box * 64, j0, kvrow);
-        tma_load_3d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvrow);
+      if (!p.q8) {
+        prefetch_tmap(&p.tm_k);
+        prefetch_tmap(&p.tm_v);
+        mbar_arrive_expect_tx(bar_kv, 2 * C::KV_TILE);
+        for (int box = 0; box < D / 64; ++box) {
+          tma_load_3d(smem + C::OFF_K + box * C::KV_BOX, &p.tm_k, bar_kv, box * 64, j0, kvrow);
+          tma_load_3d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvrow);
+        }
       }
       uint32_t used_mask = 0, phase_mask = 0;
       StepIter it;
@@ -436,6 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       row_hi = min(row_hi, (long long)j - s.q_offset + s.window);
     }
 
+    if (p.q8) {
+      // the CTA's K and V tiles, dequantized once by these eight warps into the bf16 operand tiles
+      const int tid = threadIdx.x - 128;
+      const size_t kvrow0 = (size_t)(b * s.Hkv + kvh) * s.Sk;
+      dequant_q8_tile<D>(p.kq, p.kd, kvrow0, j0, s.Sk, smem + C::OFF_K, 0, kBN, tid, 256);
+      dequant_q8_tile<D>(p.vq, p.vd, kvrow0, j0, s.Sk, smem + C::OFF_V, 0, kBN, tid, 256);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_kv);
+    }
     StepIter it;
     it.init(G, iend, BQ, ibeg, s.deterministic != 0);
     int st = 0;
@@ -774,11 +794,20 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   using C = BwdCfg<D>;
   const Shape& s = a.s;
   BwdTcParams p;
+  memset(&p, 0, sizeof(p));
   cudaError_t e;
   if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
   if ((e = make_tmap_bhsd(&p.tm_do, a.dO, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  p.q8 = a.kq != nullptr ? 1 : 0;
+  if (p.q8) {
+    p.kq = a.kq;
+    p.kd = static_cast<const __half*>(a.kd);
+    p.vq = a.vq;
+    p.vd = static_cast<const __half*>(a.vd);
+  } else {
+    if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  }
   float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
   const int groups = dq_groups(s);
   if ((e = make_tmap_f32_bhsd(&p.tm_dq, dq_acc, s.Sq, groups * s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;

@@ -20,11 +20,13 @@ LIB_PATH = os.path.join(_PKG, "libfa_train.so")
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA = range(5)
 FA_F32, FA_BF16 = 0, 1
 FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
+FA_KV_DTYPE, FA_KV_Q8_0 = 0, 1
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
             "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc", "fa_train_selftest_wait",
-            "fa_set_rows_backward", "fa_train_bwd_accum_rows")
+            "fa_set_rows_backward", "fa_train_bwd_accum_rows", "fa_train_fwd_q8", "fa_train_bwd_q8",
+            "fa_train_bwd_accum_q8")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -33,7 +35,13 @@ class FaParams(ctypes.Structure):
                 ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("mask_kind", ctypes.c_int32), ("mask_batch", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("q_offset", ctypes.c_int64), ("deterministic", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("q_offset", ctypes.c_int64), ("deterministic", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+
+
+class FaKvQ8(ctypes.Structure):
+    """fa_kv_q8: device pointers of a q8_0 K/V cache (int8 values, fp16 scales per 32 features)."""
+    _fields_ = [("k_q", ctypes.c_void_p), ("k_d", ctypes.c_void_p), ("v_q", ctypes.c_void_p),
+                ("v_d", ctypes.c_void_p)]
 
 
 class FaError(RuntimeError):
@@ -84,6 +92,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_set_rows_backward.restype = st
     lib.fa_train_bwd_accum_rows.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, sz, vp]
     lib.fa_train_bwd_accum_rows.restype = st
+    KV = ctypes.POINTER(FaKvQ8)
+    lib.fa_train_fwd_q8.argtypes = [P, vp, KV, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_fwd_q8.restype = st
+    lib.fa_train_bwd_q8.argtypes = [P, vp, KV, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_bwd_q8.restype = st
+    lib.fa_train_bwd_accum_q8.argtypes = [P, vp, KV, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_train_bwd_accum_q8.restype = st
     _lib = lib
     return lib
 
@@ -128,7 +143,8 @@ def _mask_view(mask: Optional[torch.Tensor]):
 
 def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] = None, *,
                 scale: Optional[float] = None, causal: bool = False,
-                q_offset: Optional[int] = None, window: int = 0, deterministic: bool = False) -> FaParams:
+                q_offset: Optional[int] = None, window: int = 0, deterministic: bool = False,
+                kv_format: int = FA_KV_DTYPE) -> FaParams:
     """Fill fa_params from tensor shapes. q: [B,Hq,Sq,D], k: [B,Hkv,Sk,D].
 
     q_offset (causal or windowed) defaults to Sk - Sq: the query rows are the last Sq
@@ -143,7 +159,7 @@ def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] =
     if q_offset is None:
         q_offset = Sk - Sq if (causal or window > 0) else 0
     return FaParams(B, Hq, Hkv, Sq, Sk, D, _dtype_code(q), float(scale), int(bool(causal)), kind, mb,
-                    int(window), int(q_offset), int(bool(deterministic)), 0)
+                    int(window), int(q_offset), int(bool(deterministic)), int(kv_format))
 
 
 def fwd_workspace_size(p: FaParams) -> int:
@@ -256,6 +272,58 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
                                        _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), int(rows_begin), int(n_rows),
                                        _ptr(dk_rows), _ptr(dv_rows), _ptr(ws), ws_bytes, _stream(q.device, stream)))
     return dq, dk_rows, dv_rows
+
+
+def _kv_q8(k_q, k_d, v_q, v_d) -> FaKvQ8:
+    _need_cuda(k_q, k_d, v_q, v_d)
+    if k_q.dtype != torch.int8 or v_q.dtype != torch.int8:
+        raise TypeError("k_q and v_q must be int8 [B, Hkv, Sk, D]")
+    if k_d.dtype != torch.float16 or v_d.dtype != torch.float16:
+        raise TypeError("k_d and v_d must be float16 [B, Hkv, Sk, D / 32]")
+    return FaKvQ8(k_q.data_ptr(), k_d.data_ptr(), v_q.data_ptr(), v_d.data_ptr())
+
+
+def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offset=None, window=0, out=None,
+           lse=None, workspace=None, stream=None):
+    """Forward over a q8_0 K/V cache (int8 values k_q/v_q, fp16 scales k_d/v_d per 32 features)."""
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, mview)
+    kv = _kv_q8(k_q, k_d, v_q, v_d)
+    p = make_params(q, k_q, mask, scale=scale, causal=causal, q_offset=q_offset, window=window, kv_format=FA_KV_Q8_0)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = fwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    _check(lib.fa_train_fwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(out), _ptr(lse),
+                               _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    return out, lse
+
+
+def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0,
+           deterministic=False, dq=None, dk=None, dv=None, dk_acc=None, dv_acc=None, workspace=None, stream=None):
+    """Backward over a q8_0 K/V cache. With dk_acc/dv_acc (fp32) the gradients of the dequantized
+    K/V are added into them (returns dQ); otherwise returns (dQ, dK, dV) in q's dtype."""
+    lib = load_library()
+    mview, _, _ = _mask_view(mask)
+    _need_cuda(q, o, lse, do, mview, dk_acc, dv_acc)
+    kv = _kv_q8(k_q, k_d, v_q, v_d)
+    p = make_params(q, k_q, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
+                    deterministic=deterministic, kv_format=FA_KV_Q8_0)
+    dq = torch.empty_like(q) if dq is None else dq
+    ws_bytes = bwd_workspace_size(p)
+    ws = _workspace(ws_bytes, q.device, workspace)
+    if dk_acc is not None:
+        _check(lib.fa_train_bwd_accum_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
+                                         _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
+                                         _stream(q.device, stream)))
+        return dq
+    shape = tuple(k_q.shape)
+    dk = torch.empty(shape, dtype=q.dtype, device=q.device) if dk is None else dk
+    dv = torch.empty(shape, dtype=q.dtype, device=q.device) if dv is None else dv
+    _check(lib.fa_train_bwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
+                               _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    return dq, dk, dv
 
 
 def set_rows_backward(acc: torch.Tensor, idx: torch.Tensor, out_dtype=torch.bfloat16, out=None, stream=None):

@@ -44,6 +44,7 @@ class Workload:
     causal: bool = False
     q_offset: int = 0            # query row i sits at key position q_offset + i
     window: int = 0              # sliding window half-width (0 = none)
+    kv_format: str = "bf16"      # "bf16" (K/V in dtype) or "q8_0" (8-bit values + fp16 scale per 32 features)
     mask: str = "none"           # none | extra_row | pad_self | cross | random_bool | random_add
     accum: bool = False          # dK/dV accumulate into prefilled fp32 buffers
     do_std: float = 1.0          # standard deviation of dO
@@ -77,7 +78,10 @@ WORKLOADS = [TINY_F32, DIT_SELF, DIT_CROSS, CAUSAL_LM, LONG_WINDOW]
 DIT_SELF_WINDOW = Workload("dit_self_window128_gqa_pad_s1024_d64", B=1, Hq=16, Hkv=8, Sq=1024, Sk=1024, D=64,
                            window=128, mask="pad_self", seed=1006)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [DIT_SELF_WINDOW]}
+# The long-window chunk over a q8_0 K/V cache read in place (the cache format the walk trains in).
+LONG_WINDOW_Q8 = LONG_WINDOW.with_(name="chunk512_window67584_h16_kv4_d128_accum_q8cache", kv_format="q8_0")
+
+BY_NAME = {w.name: w for w in WORKLOADS + [DIT_SELF_WINDOW, LONG_WINDOW_Q8]}
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -168,11 +172,28 @@ def make_inputs(w: Workload) -> dict:
     if w.dtype == "bf16":
         q, k, v, do = (round_to_bf16(t) for t in (q, k, v, do))
     out = {"q": q, "k": k, "v": v, "do": do}
+    if w.kv_format == "q8_0":
+        out["k_q8"] = quantize_q8_0(k)
+        out["v_q8"] = quantize_q8_0(v)
     out["mask"], out["mask_kind"] = make_mask(w)
     if w.accum:
         out["dk_acc"] = _normal(rng, (w.B, w.Hkv, w.Sk, w.D), w.acc_std)
         out["dv_acc"] = _normal(rng, (w.B, w.Hkv, w.Sk, w.D), w.acc_std)
     return out
+
+
+def quantize_q8_0(x: np.ndarray):
+    """Encode float32 [..., D] as a q8_0-style cache: per block of 32 features a float16 scale
+    d = max|x| / 127 and int8 values q = round(x / d) (computed with the stored float16 d,
+    clipped to [-127, 127]). Returns (q int8 [..., D], d float16 [..., D / 32])."""
+    x = np.asarray(x, dtype=np.float32)
+    blocks = x.reshape(*x.shape[:-1], x.shape[-1] // 32, 32)
+    d = (np.abs(blocks).max(axis=-1) / np.float32(127.0)).astype(np.float16)
+    dd = d.astype(np.float32)[..., None]
+    safe = np.where(dd > 0, dd, np.float32(1.0))
+    q = np.where(dd > 0, np.rint(blocks / safe), 0.0)
+    q = np.clip(q, -127, 127).astype(np.int8)
+    return q.reshape(x.shape), d
 
 
 def visible_pairs(w: Workload) -> int:

@@ -179,15 +179,19 @@ def oracle_sample(w: wl.Workload, inputs: dict, n_heads: int):
     n_heads = max(1, min(n_heads, w.Hq))
     kv = sorted({h // G for h in range(n_heads)})
     q, do = inputs["q"][:1, :n_heads], inputs["do"][:1, :n_heads]
-    k, v = inputs["k"][:1, kv], inputs["v"][:1, kv]
-    # the sample keeps the GQA mapping: n_heads query heads over their kv heads
-    if len(kv) * G != n_heads:
-        k = np.repeat(k, G, axis=1)[:, :n_heads]
-        v = np.repeat(v, G, axis=1)[:, :n_heads]
     mask = inputs["mask"]
     if mask is not None:
         mask = mask[:1]
     t0 = time.perf_counter()
+    if w.kv_format == "q8_0":   # the cache is read as its values, inside the timed sample
+        k = ref.dequantize_q8_0(inputs["k_q8"][0][:1, kv], inputs["k_q8"][1][:1, kv])
+        v = ref.dequantize_q8_0(inputs["v_q8"][0][:1, kv], inputs["v_q8"][1][:1, kv])
+    else:
+        k, v = inputs["k"][:1, kv], inputs["v"][:1, kv]
+    # the sample keeps the GQA mapping: n_heads query heads over their kv heads
+    if len(kv) * G != n_heads:
+        k = np.repeat(k, G, axis=1)[:, :n_heads]
+        v = np.repeat(v, G, axis=1)[:, :n_heads]
     ref.backward(q, k, v, do, w.scale, mask, inputs["mask_kind"], w.causal, w.q_offset, w.window)
     dt = time.perf_counter() - t0
     pairs_per_head = wl.visible_pairs(w.with_(B=1, Hq=1, Hkv=1))
@@ -251,13 +255,19 @@ def run_ours(args):
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     es = 2 if w.dtype == "bf16" else 4
 
-    host = {n: torch.from_numpy(inputs[n]).to(dt).pin_memory() for n in ("q", "k", "v", "do")}
+    q8 = w.kv_format == "q8_0"
+    host = {n: torch.from_numpy(inputs[n]).to(dt).pin_memory() for n in (("q", "do") if q8 else ("q", "k", "v", "do"))}
+    if q8:   # the K/V cache in its own format: int8 values and fp16 scales, read in place
+        for n in ("k", "v"):
+            qv, dv_ = inputs[n + "_q8"]
+            host[n + "_q"] = torch.from_numpy(qv).pin_memory()
+            host[n + "_d"] = torch.from_numpy(dv_).pin_memory()
     if inputs["mask"] is not None:
         host["mask"] = torch.from_numpy(inputs["mask"]).pin_memory()
     d = {n: t.to(dev) for n, t in host.items()}
     mask = d.get("mask")
     kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=args.deterministic)
-    p = ft.make_params(d["q"], d["k"], mask, **kw)
+    p = ft.make_params(d["q"], d["k_q" if q8 else "k"], mask, **kw)
     ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     o = torch.empty_like(d["q"])
@@ -272,17 +282,36 @@ def run_ours(args):
         dk_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
         dv_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
     else:
-        dk, dv = torch.empty_like(d["k"]), torch.empty_like(d["v"])
+        kv_shape = (w.B, w.Hkv, w.Sk, w.D)
+        dk, dv = torch.empty(kv_shape, dtype=dt, device=dev), torch.empty(kv_shape, dtype=dt, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fkw = {k_: v_ for k_, v_ in kw.items() if k_ != "deterministic"}
+
+    def fwd_call(src, o_, lse_):
+        if q8:
+            return ft.fwd_q8(src["q"], src["k_q"], src["k_d"], src["v_q"], src["v_d"], src.get("mask"), out=o_,
+                             lse=lse_, workspace=ws_f, **fkw)
+        return ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=o_, lse=lse_, workspace=ws_f, **kw)
+
+    def bwd_call(src, o_, lse_, dq_, dk_, dv_):
+        if q8:
+            kv = (src["k_q"], src["k_d"], src["v_q"], src["v_d"])
+            if w.accum:
+                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk_acc=dk_, dv_acc=dv_,
+                          workspace=ws_b, **kw)
+            else:
+                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
+                          workspace=ws_b, **kw)
+        elif w.accum:
+            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, w.q_offset, w.Sq,
+                              src.get("mask"), dq=dq_, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
+        else:
+            ft.bwd(src["q"], src["k"], src["v"], o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
+                   workspace=ws_b, **kw)
 
     def step(src):
-        ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=o, lse=lse, workspace=ws_f, **kw)
-        if w.accum:
-            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o, lse, src["do"], dk, dv, w.q_offset, w.Sq,
-                              src.get("mask"), dq=dq, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
-        else:
-            ft.bwd(src["q"], src["k"], src["v"], o, lse, src["do"], src.get("mask"), dq=dq, dk=dk, dv=dv,
-                   workspace=ws_b, **kw)
+        fwd_call(src, o, lse)
+        bwd_call(src, o, lse, dq, dk, dv)
 
     fl = wl.flops(w)
     clocks = ClockSampler(local)
@@ -384,15 +413,9 @@ def run_ours(args):
         if i >= 2:
             comp.wait_event(read_back[sl])          # step i-2's results have been read back
         src = bufs[sl]
-        o_, lse_ = ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=fwd_outs[sl][0], lse=fwd_outs[sl][1],
-                          workspace=ws_f, **kw)
+        o_, lse_ = fwd_call(src, fwd_outs[sl][0], fwd_outs[sl][1])
         dq_, dk_, dv_ = outs[sl]
-        if w.accum:
-            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, w.q_offset, w.Sq,
-                              src.get("mask"), dq=dq_, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
-        else:
-            ft.bwd(src["q"], src["k"], src["v"], o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
-                   workspace=ws_b, **kw)
+        bwd_call(src, o_, lse_, dq_, dk_, dv_)
         done[sl].record(comp)
         with torch.cuda.stream(copy_out):
             copy_out.wait_event(done[sl])
@@ -429,7 +452,8 @@ def run_ours(args):
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask, "accum": w.accum,
-                   "rows_read_back": [w.q_offset, w.Sq] if w.accum else None,
+                   "rows_read_back": [w.q_offset, w.Sq] if w.accum and not q8 else None,
+                   "kv_format": w.kv_format,
                    "deterministic": bool(args.deterministic),
                    "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
                    "l2": "flushed (256 MiB write) between timed steps, outside the step events",

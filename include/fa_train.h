@@ -83,6 +83,11 @@ typedef enum fa_mask_kind {
   FA_MASK_BOOL_U8 = 2  /* uint8 boolean mask, nonzero = attend */
 } fa_mask_kind;
 
+typedef enum fa_kv_format {
+  FA_KV_DTYPE = 0, /* K and V are tensors in p->dtype */
+  FA_KV_Q8_0 = 1   /* K and V are a q8_0 cache (fa_kv_q8, the _q8 entry points) */
+} fa_kv_format;
+
 typedef struct fa_params {
   int32_t B;          /* batch, >= 1 */
   int32_t Hq;         /* query heads, a multiple of Hkv */
@@ -100,8 +105,9 @@ typedef struct fa_params {
                          q_offset + Sq <= Sk. Ignored (taken as 0) when neither is set. */
   int32_t deterministic; /* 0 or 1. 1: the backward's dQ is bitwise reproducible from run to run
                             (its per-key-tile partials are added in a fixed order); dK/dV always are.
-                            Costs some backward speed and a few bytes of workspace. */
-  int32_t reserved;   /* must be 0 */
+                            Costs some backward speed and workspace. */
+  int32_t kv_format;  /* fa_kv_format: FA_KV_DTYPE for the plain entry points, FA_KV_Q8_0 for the
+                         _q8 ones (it sizes the workspace) */
 } fa_params;
 
 /* Bytes of scratch the forward needs for these parameters (0 when none). */
@@ -138,6 +144,42 @@ FA_API fa_status fa_train_bwd_accum(const fa_params* p, const void* q, const voi
                              const void* mask, const void* o, const float* lse, const void* dO,
                              void* dq, float* dk_acc, float* dv_acc, void* ws, size_t ws_bytes,
                              void* stream);
+
+/*
+ * A q8_0-style quantized K/V cache, read in place (llama.cpp PR #57, commit 2394a4c: a q8_0
+ * cache trains in place; the backward admits a quantized source where it only casts a tile).
+ * Per (batch, key/value head, key) the cache holds D signed 8-bit values and one fp16 scale per
+ * block of 32 consecutive features; the value is x[d] = scale[d / 32] * q[d] (the layout of
+ * ggml's q8_0 blocks, split into a value plane and a scale plane). This struct lives in host
+ * memory; its pointers are DEVICE pointers, 16-byte aligned:
+ *   k_q, v_q: int8 [B, Hkv, Sk, D]; k_d, v_d: fp16 (IEEE binary16 bits) [B, Hkv, Sk, D / 32].
+ */
+typedef struct fa_kv_q8 {
+  const int8_t* k_q;
+  const uint16_t* k_d;
+  const int8_t* v_q;
+  const uint16_t* v_d;
+} fa_kv_q8;
+
+/*
+ * The op with K and V read from a q8_0 cache (the _q8 entry points): as fa_train_fwd /
+ * fa_train_bwd / fa_train_bwd_accum with `k`, `v` replaced by `kv`, and p->kv_format ==
+ * FA_KV_Q8_0. The values are rounded to bf16 (x = scale * q, to nearest even) and the op then
+ * computes exactly as on a bf16 K/V: the backward dequantizes each CTA's key tile on chip, in
+ * place; the forward, whose key tiles are read by every query tile, first dequantizes the cache
+ * once into a bf16 copy in its workspace (2 x B x Hkv x Sk x D x 2 bytes, included in
+ * fa_train_fwd_workspace_size). dK and dV are the gradients with respect to the dequantized
+ * values (bf16 [B, Hkv, Sk, D] for fa_train_bwd_q8, added into fp32 buffers for
+ * fa_train_bwd_accum_q8). Needs p->dtype == FA_BF16 (else FA_ERR_UNSUPPORTED).
+ */
+FA_API fa_status fa_train_fwd_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask,
+                                 void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+FA_API fa_status fa_train_bwd_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask,
+                                 const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                 void* ws, size_t ws_bytes, void* stream);
+FA_API fa_status fa_train_bwd_accum_q8(const fa_params* p, const void* q, const fa_kv_q8* kv, const void* mask,
+                                       const void* o, const float* lse, const void* dO, void* dq, float* dk_acc,
+                                       float* dv_acc, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * SET_ROWS backward: the gradient of the rows a chunk wrote into its cached K/V window

@@ -102,6 +102,14 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def dequantize_q8_0(q, d) -> np.ndarray:
+    """Values of a q8_0-style K/V cache (llama.cpp PR #57, commit 2394a4c: a q8_0 cache is read in
+    place): feature f of a row is d[f // 32] * q[f], q int8 [..., D], d float16 [..., D / 32]."""
+    q = np.asarray(q, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float16).astype(np.float64)
+    return q * np.repeat(d, 32, axis=-1)
+
+
 def forward(q, k, v, scale, mask=None, mask_kind="none", causal=False, q_offset=0, window=0):
     """Return O [B,Hq,Sq,D] and LSE [B,Hq,Sq], both float64."""
     q, k, v = _as64(q), _as64(k), _as64(v)

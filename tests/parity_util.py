@@ -26,17 +26,32 @@ def to_device(inputs: dict, w: wl.Workload, device="cuda"):
     if w.accum:
         t["dk_acc"] = torch.from_numpy(inputs["dk_acc"]).to(device).contiguous()
         t["dv_acc"] = torch.from_numpy(inputs["dv_acc"]).to(device).contiguous()
+    if w.kv_format == "q8_0":
+        for n in ("k", "v"):
+            qv, dv = inputs[n + "_q8"]
+            t[n + "_q"] = torch.from_numpy(qv).to(device).contiguous()
+            t[n + "_d"] = torch.from_numpy(dv).to(device).contiguous()
     return t
 
 
 def run_gpu(w: wl.Workload, t: dict, deterministic: bool = False) -> dict:
     """Forward + backward on the GPU; returns float64 numpy copies of every output."""
     kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=deterministic)
-    o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
-    if w.accum:
+    if w.kv_format == "q8_0":
+        kv = (t["k_q"], t["k_d"], t["v_q"], t["v_d"])
+        fkw = {k_: v_ for k_, v_ in kw.items() if k_ != "deterministic"}
+        o, lse = ft.fwd_q8(t["q"], *kv, t["mask"], **fkw)
+        if w.accum:
+            dk, dv = t["dk_acc"].clone(), t["dv_acc"].clone()
+            dq = ft.bwd_q8(t["q"], *kv, o, lse, t["do"], t["mask"], dk_acc=dk, dv_acc=dv, **kw)
+        else:
+            dq, dk, dv = ft.bwd_q8(t["q"], *kv, o, lse, t["do"], t["mask"], **kw)
+    elif w.accum:
+        o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
         dk, dv = t["dk_acc"].clone(), t["dv_acc"].clone()
         dq = ft.bwd_accum(t["q"], t["k"], t["v"], o, lse, t["do"], dk, dv, t["mask"], **kw)
     else:
+        o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
         dq, dk, dv = ft.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], t["mask"], **kw)
     torch.cuda.synchronize()
     status = ft.device_status()
@@ -47,6 +62,9 @@ def run_gpu(w: wl.Workload, t: dict, deterministic: bool = False) -> dict:
 def run_oracle(w: wl.Workload, inputs: dict, q_heads=None, kv_heads=None) -> dict:
     """Oracle on all heads, or on the given query heads and the key/value heads they read."""
     q, k, v, do = inputs["q"], inputs["k"], inputs["v"], inputs["do"]
+    if w.kv_format == "q8_0":
+        k = ref.dequantize_q8_0(*inputs["k_q8"])
+        v = ref.dequantize_q8_0(*inputs["v_q8"])
     if q_heads is not None:
         q, do = q[:, q_heads], do[:, q_heads]
         k, v = k[:, kv_heads], v[:, kv_heads]
@@ -65,7 +83,7 @@ def max_err(got, exp):
     return float(np.abs(got - exp).max()) if got.size else 0.0
 
 
-def assert_parity(w: wl.Workload, got: dict, exp: dict, where: str = ""):
+def assert_parity(w: wl.Workload, got: dict, exp: dict, where: str = "", lse_extra: float = 0.0):
     """Max-abs error of O, dQ, dK, dV within rel * max|ref| + abs; LSE within LSE_ABS absolute.
 
     With one key per head, softmax is constant (P = 1), so dQ and dK are exactly
@@ -80,7 +98,7 @@ def assert_parity(w: wl.Workload, got: dict, exp: dict, where: str = ""):
     for n in (("dv",) if w.Sk == 1 else ("dq", "dk", "dv")):
         assert float(np.abs(exp[n]).max()) > 0, f"{n} reference is vacuously zero"
     e = max_err(got["lse"], exp["lse"])
-    assert e <= LSE_ABS, f"{w.name}{where}: lse max-abs err {e:.3e}"
+    assert e <= LSE_ABS + lse_extra, f"{w.name}{where}: lse max-abs err {e:.3e} (allowed {LSE_ABS + lse_extra:.3e})"
 
 
 def assert_exact_zeros(w: wl.Workload, inputs: dict, got: dict, q_heads=None):

@@ -50,13 +50,13 @@ def test_struct_layout_matches_header(tmp_path):
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "fa_train.h"\n'
                    'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(fa_params), offsetof(fa_params, scale),'
                    ' offsetof(fa_params, mask_batch), offsetof(fa_params, q_offset), offsetof(fa_params, deterministic),'
-                   ' offsetof(fa_params, reserved), sizeof(fa_status));return 0;}\n')
+                   ' offsetof(fa_params, kv_format), sizeof(fa_status));return 0;}\n')
     exe = tmp_path / "layout"
     subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     P = ft.FaParams
     assert [int(x) for x in got] == [ctypes.sizeof(P), P.scale.offset, P.mask_batch.offset, P.q_offset.offset,
-                                     P.deterministic.offset, P.reserved.offset, ctypes.sizeof(ctypes.c_int)]
+                                     P.deterministic.offset, P.kv_format.offset, ctypes.sizeof(ctypes.c_int)]
 
 
 def good_params(**kw):
@@ -81,7 +81,7 @@ BAD = [
     ("mask_batch", dict(mask_kind=ft.FA_MASK_ADD_F32, mask_batch=3), ft.FA_ERR_INVALID_ARG),
     ("window_negative", dict(window=-1), ft.FA_ERR_INVALID_ARG),
     ("deterministic2", dict(deterministic=2), ft.FA_ERR_INVALID_ARG),
-    ("reserved", dict(reserved=1), ft.FA_ERR_INVALID_ARG),
+    ("kv_format", dict(kv_format=2), ft.FA_ERR_INVALID_ARG),
     ("window_offset_too_big", dict(window=8, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_too_big", dict(causal=1, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_negative", dict(causal=1, q_offset=-1), ft.FA_ERR_INVALID_ARG),
@@ -145,3 +145,14 @@ def test_status_strings(lib):
     for code in range(5):
         assert lib.fa_status_str(code)
     assert lib.fa_status_str(99) == b"unknown status"
+
+
+def test_kv_format_must_match_the_entry_point(lib):
+    p = good_params(kv_format=ft.FA_KV_Q8_0)
+    fake = 1 << 20
+    st = lib.fa_train_fwd(ctypes.byref(p), fake, fake, fake, None, fake, fake, None, 0, None)
+    assert st == ft.FA_ERR_INVALID_ARG and b"_q8" in lib.fa_last_error()
+    # the q8 forward's workspace holds the dequantized bf16 K and V
+    plain = good_params()
+    extra = lib.fa_train_fwd_workspace_size(ctypes.byref(p)) - lib.fa_train_fwd_workspace_size(ctypes.byref(plain))
+    assert extra >= 2 * 1 * 2 * 130 * 64 * 2

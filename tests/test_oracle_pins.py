@@ -414,3 +414,44 @@ def test_bf16_rounding_matches_torch_including_ties():
     for v in (x, ties, ties_odd, np.array([0.0, -0.0, 1.0, -3.5, 1e-40], np.float32), x.reshape(4, 8, 128)):
         want = torch.tensor(v).to(torch.bfloat16).float().numpy()
         np.testing.assert_array_equal(rows_ref.to_bf16_bits(v), want)
+
+
+# ---- q8_0 K/V cache ----------------------------------------------------------------------------
+
+def test_q8_0_dequantization_uses_one_scale_per_32_features():
+    """Block f // 32 of each row scales features [32 b, 32 b + 32): distinct scales per block and
+    unit values give each scale repeated 32 times; a row-major slip or a transposed block fails."""
+    q = np.ones((2, 3, 128), np.int8)
+    q[1, 2, 70] = -5
+    d = (np.arange(2 * 3 * 4, dtype=np.float64).reshape(2, 3, 4) + 1.0).astype(np.float16) / 8
+    got = ref.dequantize_q8_0(q, d)
+    want = np.repeat(d.astype(np.float64), 32, axis=-1)
+    want[1, 2, 70] *= -5
+    np.testing.assert_array_equal(got, want)
+
+
+def test_q8_0_encoding_round_trip_is_within_half_a_step():
+    """The cache encoding of the seeded inputs: |x - d q| <= d / 2 per element (plus the float16
+    rounding of d, which can push max|x| / d a hair past 127)."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((2, 4, 50, 128)).astype(np.float32)
+    q, d = wl.quantize_q8_0(x)
+    back = ref.dequantize_q8_0(q, d)
+    step = np.repeat(d.astype(np.float64), 32, axis=-1)
+    amax = np.repeat(np.abs(x.reshape(2, 4, 50, 4, 32)).max(-1), 32, axis=-1)
+    assert np.all(np.abs(back - x) <= step / 2 + amax * 2.0 ** -10)
+
+
+def test_attention_on_a_q8_0_cache_is_attention_on_its_values():
+    """The op over the cache equals the op over the dequantized K/V (so the gradients are those of
+    the cache's values), checked against PyTorch float64 SDPA with autograd."""
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((1, 2, 5, 32))
+    kq, kd = wl.quantize_q8_0(rng.standard_normal((1, 1, 9, 32)).astype(np.float32))
+    vq, vd = wl.quantize_q8_0(rng.standard_normal((1, 1, 9, 32)).astype(np.float32))
+    g = rng.standard_normal((1, 2, 5, 32))
+    k, v = ref.dequantize_q8_0(kq, kd), ref.dequantize_q8_0(vq, vd)
+    r = ref.backward(q, k, v, g, 0.3, causal=True, q_offset=4)
+    o, dq, dk, dv = _sdpa_fp64(q, k, v, g, 0.3, None, "none", True, 4)
+    for a, b in ((r["o"], o), (r["dq"], dq), (r["dk"], dk), (r["dv"], dv)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
