@@ -57,6 +57,10 @@ fa_status check_params(const fa_params* p, Shape& s) {
   if (p->kv_format != FA_KV_DTYPE && p->kv_format != FA_KV_Q8_0) {
     set_error("kv_format=%d invalid", p->kv_format); return FA_ERR_INVALID_ARG;
   }
+  if (p->layout != FA_LAYOUT_BHSD && p->layout != FA_LAYOUT_BSHD) {
+    set_error("layout=%d invalid", p->layout); return FA_ERR_INVALID_ARG;
+  }
+  if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
   const bool positioned = p->causal || p->window > 0;
   if (positioned && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
     set_error("q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
@@ -72,6 +76,7 @@ fa_status check_params(const fa_params* p, Shape& s) {
   s.q_offset = (p->causal || s.window > 0) ? (long long)p->q_offset : 0;
   s.deterministic = p->deterministic;
   s.kv_q8 = p->kv_format == FA_KV_Q8_0 ? 1 : 0;
+  s.layout = p->layout;
   return FA_OK;
 }
 
@@ -295,6 +300,7 @@ static fa_status fwd_common(const fa_params* p, const void* q, const KvIn& kv, c
     if (e != cudaSuccess) return cuda_status(e, "q8_0 dequantize launch");
     a.k = kbf;
     a.v = vbf;
+    a.kv_layout = 0;   // the copy is [B, Hkv, Sk, D] like the cache's planes
   }
   e = plan.tensor_core ? tc_fwd(a, plan, (char*)ws) : simt_fwd(a);
   return cuda_status(e, "forward launch");

@@ -52,21 +52,26 @@ __device__ __forceinline__ void store8(float* p, const float* x) {
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, const T* __restrict__ dO,
                                                    float* __restrict__ dsum, float* __restrict__ dq_acc,
-                                                   long long rows, int groups) {
+                                                   long long rows, int groups, const Shape s) {
   constexpr int LPR = D / 8;  // lanes per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = tid / LPR;
+  const long long row = tid / LPR;   // over [B, Hq, Sq], like D and the dQ accumulators
   const int part = (int)(tid % LPR);
   float acc = 0.f;
   if (row < rows) {
+    size_t at = (size_t)row * D;   // [B, Hq, Sq, D]: the row's offset directly
+    if (s.layout) {
+      const long long bh = row / s.Sq, i = row % s.Sq;
+      at = head_base(s, (int)(bh / s.Hq), (int)(bh % s.Hq), s.Hq, s.Sq) + (size_t)i * row_stride(s, s.Hq);
+    }
     float a[8], g[8];
-    load8(o + row * D + part * 8, a);
-    load8(dO + row * D + part * 8, g);
+    load8(o + at + part * 8, a);
+    load8(dO + at + part * 8, g);
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc = fmaf(a[t], g[t], acc);
     if (dq_acc != nullptr) {
       const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int g = 0; g < groups; ++g) store8(dq_acc + ((long long)g * rows + row) * D + part * 8, z);
+      for (int gi = 0; gi < groups; ++gi) store8(dq_acc + ((long long)gi * rows + row) * D + part * 8, z);
     }
   }
 #pragma unroll
@@ -76,9 +81,16 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, cons
 
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
-                                                         float scale, long long vecs, int groups) {
+                                                         float scale, long long vecs, int groups, const Shape s) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= vecs) return;
+  const long long e = i * 8;   // element of the accumulator, [B, Hq, Sq, D]
+  size_t at = (size_t)e;        // the same element of dQ when dQ is [B, Hq, Sq, D] too
+  if (s.layout) {
+    const long long row = e / s.D, bh = row / s.Sq, qi = row % s.Sq;
+    at = head_base(s, (int)(bh / s.Hq), (int)(bh % s.Hq), s.Hq, s.Sq) + (size_t)qi * row_stride(s, s.Hq) +
+         (size_t)(e % s.D);
+  }
   float x[8];
   load8(acc + i * 8, x);
   for (int g = 1; g < groups; ++g) {   // the key-tile groups' accumulators, always in group order
@@ -89,7 +101,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   }
 #pragma unroll
   for (int t = 0; t < 8; ++t) x[t] *= scale;
-  store8(dq + i * 8, x);
+  store8(dq + at, x);
 }
 
 // One block per (mask batch, q-tile, k-tile) of 128 x 128, flattened in that order.
@@ -134,17 +146,17 @@ cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, in
   if (s.dtype == DT_BF16) {
     if (s.D == 64)
       dsum_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, s);
     else
       dsum_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, s);
   } else {
     if (s.D == 64)
       dsum_kernel<float, 64><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                           dq_acc_to_zero, rows, groups);
+                                                           dq_acc_to_zero, rows, groups, s);
     else
       dsum_kernel<float, 128><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                            dq_acc_to_zero, rows, groups);
+                                                            dq_acc_to_zero, rows, groups, s);
   }
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -160,9 +172,9 @@ cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups)
   if (e != cudaSuccess) return e;
   if (s.dtype == DT_BF16)
     dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(dq_acc, (__nv_bfloat16*)a.dq, s.scale, vecs,
-                                                                   groups);
+                                                                   groups, s);
   else
-    dq_convert_kernel<float><<<blocks, 256, 0, a.stream>>>(dq_acc, (float*)a.dq, s.scale, vecs, groups);
+    dq_convert_kernel<float><<<blocks, 256, 0, a.stream>>>(dq_acc, (float*)a.dq, s.scale, vecs, groups, s);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_BWD_DQCONV, a.stream);

@@ -24,7 +24,17 @@ struct Shape {
   long long q_offset;  // key position of query row 0 (0 unless causal or windowed)
   int deterministic;   // the backward adds dQ partials in a fixed order
   int kv_q8;           // K/V come from a q8_0 cache
+  int layout;          // 0: [B, H, S, D]; 1: [B, S, H, D] (Q, K, V, O, dO, dQ, dK, dV)
 };
+
+// Offset (elements) of row 0 of head h of batch b, and the distance between consecutive rows of
+// one head, in a [B, H, S, D] or [B, S, H, D] tensor with D = s.D.
+__host__ __device__ inline size_t head_base(const Shape& s, int b, int h, int H, long long S) {
+  return s.layout ? ((size_t)b * (size_t)S * H + h) * (size_t)s.D : ((size_t)b * H + h) * (size_t)S * s.D;
+}
+__host__ __device__ inline size_t row_stride(const Shape& s, int H) {
+  return s.layout ? (size_t)H * s.D : (size_t)s.D;
+}
 
 struct FwdArgs {
   Shape s;
@@ -35,6 +45,7 @@ struct FwdArgs {
   void* o;
   float* lse;
   cudaStream_t stream;
+  int kv_layout = -1;   // layout of k, v when it differs from s.layout (a dequantized q8_0 cache)
 };
 
 struct BwdArgs {
@@ -135,7 +146,10 @@ cudaError_t launch_rows_copy(const Shape& s, const float* dk_acc, const float* d
 // tcgen05 paths (bf16, D in {64, 128}).
 bool tc_fwd_supported(const Shape& s);
 bool tc_bwd_supported(const Shape& s);
-cudaError_t make_tmap_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D, int box_rows);
+// bf16 tensor of B x H heads of S rows of D features ([B, H, S, D] when layout == 0, [B, S, H, D]
+// when 1) viewed as (D, S, H, B) with 64 x box_rows x 1 x 1 boxes and the 128-byte swizzle.
+cudaError_t make_tmap_4d(struct CUtensorMap_st* map, const void* base, int layout, int B, int H, int S, int D,
+                         int box_rows);
 cudaError_t make_tmap_f32_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D, int box_rows);
 int tc_fwd_kv_splits(const Shape& s);
 cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);

@@ -17,21 +17,26 @@ template <typename T>
 __global__ void __launch_bounds__(256) set_rows_backward_kernel(const float* __restrict__ acc, int heads, int S,
                                                                 int D, const int64_t* __restrict__ idx,
                                                                 long long row0, int n_rows, T* __restrict__ out,
-                                                                unsigned* status) {
+                                                                unsigned* status, int H, int layout) {
   const int vec = D / 4;                              // float4 per row
   const int rows_per_block = blockDim.x / vec;
   const long long g = (long long)blockIdx.x * rows_per_block + threadIdx.x / vec;   // (bh, r) flattened
   const int c = threadIdx.x % vec;
   if (threadIdx.x >= rows_per_block * vec || g >= (long long)heads * n_rows) return;
   const int bh = (int)(g / n_rows), r = (int)(g % n_rows);
+  const int b = bh / H, h = bh % H;
+  // [B, H, rows, D], or [B, rows, H, D] when layout == 1
+  auto at = [&](long long rows, long long i) -> size_t {
+    return layout ? (((size_t)b * rows + i) * H + h) * D : (((size_t)b * H + h) * rows + i) * D;
+  };
   const long long src = idx != nullptr ? __ldg(idx + r) : row0 + r;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
   if (src >= 0 && src < S) {
-    v = __ldg(reinterpret_cast<const float4*>(acc + ((size_t)bh * S + (size_t)src) * D) + c);
+    v = __ldg(reinterpret_cast<const float4*>(acc + at(S, src)) + c);
   } else if (c == 0 && status != nullptr) {
     atomicCAS(status, 0u, 0x40000000u | kSiteRowIndex);
   }
-  T* dst = out + ((size_t)bh * n_rows + r) * D + 4 * c;
+  T* dst = out + at(n_rows, r) + 4 * c;
   if constexpr (sizeof(T) == 4) {
     *reinterpret_cast<float4*>(dst) = v;
   } else {
@@ -46,7 +51,8 @@ __global__ void __launch_bounds__(256) set_rows_backward_kernel(const float* __r
 }  // namespace
 
 static cudaError_t gather_rows(const float* acc, int heads, int S, int D, const int64_t* idx, long long row0,
-                               int n_rows, void* out, int out_dtype, unsigned* status, cudaStream_t st) {
+                               int n_rows, void* out, int out_dtype, unsigned* status, cudaStream_t st, int H = 1,
+                               int layout = 0) {
   const int vec = D / 4;
   const int rows_per_block = 256 / vec;
   const long long total = (long long)heads * n_rows;
@@ -55,10 +61,10 @@ static cudaError_t gather_rows(const float* acc, int heads, int S, int D, const 
   if (blocks == 0) return cudaSuccess;
   if (out_dtype == DT_BF16)
     set_rows_backward_kernel<__nv_bfloat16><<<(unsigned)blocks, rows_per_block * vec, 0, st>>>(
-        acc, heads, S, D, idx, row0, n_rows, static_cast<__nv_bfloat16*>(out), status);
+        acc, heads, S, D, idx, row0, n_rows, static_cast<__nv_bfloat16*>(out), status, H, layout);
   else
     set_rows_backward_kernel<float><<<(unsigned)blocks, rows_per_block * vec, 0, st>>>(
-        acc, heads, S, D, idx, row0, n_rows, static_cast<float*>(out), status);
+        acc, heads, S, D, idx, row0, n_rows, static_cast<float*>(out), status, H, layout);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -70,8 +76,10 @@ cudaError_t launch_set_rows_backward(const float* acc, int heads, int S, int D, 
 
 cudaError_t launch_rows_copy(const Shape& s, const float* dk_acc, const float* dv_acc, long long row0, int n_rows,
                              void* dk_rows, void* dv_rows, cudaStream_t st) {
-  cudaError_t e = gather_rows(dk_acc, s.B * s.Hkv, s.Sk, s.D, nullptr, row0, n_rows, dk_rows, s.dtype, nullptr, st);
-  if (e == cudaSuccess) e = gather_rows(dv_acc, s.B * s.Hkv, s.Sk, s.D, nullptr, row0, n_rows, dv_rows, s.dtype, nullptr, st);
+  cudaError_t e = gather_rows(dk_acc, s.B * s.Hkv, s.Sk, s.D, nullptr, row0, n_rows, dk_rows, s.dtype, nullptr, st,
+                              s.Hkv, s.layout);
+  if (e == cudaSuccess)
+    e = gather_rows(dv_acc, s.B * s.Hkv, s.Sk, s.D, nullptr, row0, n_rows, dv_rows, s.dtype, nullptr, st, s.Hkv, s.layout);
   return e;
 }
 

@@ -38,13 +38,14 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Shape s, const T* __
   const int kvh = h / (s.Hq / s.Hkv);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * ROWS;
-  const T* qh = q + (size_t)(b * s.Hq + h) * s.Sq * D;
-  const T* kh = k + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
-  const T* vh = v + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
+  const size_t qs = row_stride(s, s.Hq), ks = row_stride(s, s.Hkv);   // row strides of one head
+  const T* qh = q + head_base(s, b, h, s.Hq, s.Sq);
+  const T* kh = k + head_base(s, b, kvh, s.Hkv, s.Sk);
+  const T* vh = v + head_base(s, b, kvh, s.Hkv, s.Sk);
 
   for (int idx = threadIdx.x; idx < ROWS * D; idx += kThreads) {
     const int r = idx / D, d = idx % D, i = row0 + r;
-    Qs[r][d] = (i < s.Sq) ? to_f(qh[(size_t)i * D + d]) : 0.f;
+    Qs[r][d] = (i < s.Sq) ? to_f(qh[(size_t)i * qs + d]) : 0.f;
   }
 
   float m[2] = {-CUDART_INF_F, -CUDART_INF_F};
@@ -66,8 +67,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Shape s, const T* __
     for (int idx = threadIdx.x; idx < KT * D; idx += kThreads) {
       const int r = idx / D, d = idx % D, j = j0 + r;
       const bool in = j < s.Sk;
-      Ks[r][d] = in ? to_f(kh[(size_t)j * D + d]) : 0.f;
-      Vs[r][d] = in ? to_f(vh[(size_t)j * D + d]) : 0.f;
+      Ks[r][d] = in ? to_f(kh[(size_t)j * ks + d]) : 0.f;
+      Vs[r][d] = in ? to_f(vh[(size_t)j * ks + d]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Shape s, const T* __
     if (i >= s.Sq) continue;
     const bool alive = l[rr] > 0.f;
     const float inv = alive ? 1.f / l[rr] : 0.f;
-    T* orow = o + ((size_t)(b * s.Hq + h) * s.Sq + i) * D;
+    T* orow = o + head_base(s, b, h, s.Hq, s.Sq) + (size_t)i * qs;
 #pragma unroll
     for (int t = 0; t < NT; ++t) from_f(orow + lane + 32 * t, acc[rr][t] * inv);
     if (lane == 0) lse[(size_t)(b * s.Hq + h) * s.Sq + i] = alive ? m[rr] + logf(l[rr]) : 0.f;
@@ -133,14 +134,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(
   const int G = s.Hq / s.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = blockIdx.x * KT;
-  const T* kh = k + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
-  const T* vh = v + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
+  const size_t qs = row_stride(s, s.Hq), ks = row_stride(s, s.Hkv);   // row strides of one head
+  const T* kh = k + head_base(s, b, kvh, s.Hkv, s.Sk);
+  const T* vh = v + head_base(s, b, kvh, s.Hkv, s.Sk);
 
   for (int idx = threadIdx.x; idx < KT * D; idx += kThreads) {
     const int r = idx / D, d = idx % D, j = j0 + r;
     const bool in = j < s.Sk;
-    Ks[r][d] = in ? to_f(kh[(size_t)j * D + d]) : 0.f;
-    Vs[r][d] = in ? to_f(vh[(size_t)j * D + d]) : 0.f;
+    Ks[r][d] = in ? to_f(kh[(size_t)j * ks + d]) : 0.f;
+    Vs[r][d] = in ? to_f(vh[(size_t)j * ks + d]) : 0.f;
   }
 
   float dk[KPW][NT], dv[KPW][NT];
@@ -158,14 +160,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(
 
   for (int hh = 0; hh < G; ++hh) {
     const int h = kvh * G + hh;
-    const size_t rowbase = (size_t)(b * s.Hq + h) * s.Sq;
+    const size_t rowbase = (size_t)(b * s.Hq + h) * s.Sq;   // LSE and D rows
+    const size_t qbase = head_base(s, b, h, s.Hq, s.Sq);
     for (int i0 = ibeg; i0 < s.Sq; i0 += QT) {
       __syncthreads();
       for (int idx = threadIdx.x; idx < QT * D; idx += kThreads) {
         const int r = idx / D, d = idx % D, i = i0 + r;
         const bool in = i < s.Sq;
-        Qs[r][d] = in ? to_f(q[(rowbase + i) * D + d]) : 0.f;
-        dOs[r][d] = in ? to_f(dO[(rowbase + i) * D + d]) : 0.f;
+        Qs[r][d] = in ? to_f(q[qbase + (size_t)i * qs + d]) : 0.f;
+        dOs[r][d] = in ? to_f(dO[qbase + (size_t)i * qs + d]) : 0.f;
       }
       if (threadIdx.x < QT) {
         const int i = i0 + threadIdx.x;
@@ -204,11 +207,11 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt_kernel(
   for (int kk = 0; kk < KPW; ++kk) {
     const int j = j0 + warp * KPW + kk;
     if (j >= s.Sk) continue;
-    const size_t base = ((size_t)(b * s.Hkv + kvh) * s.Sk + j) * D;
+    const size_t base = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)j * ks;
     // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
     const long long rr = (long long)j - rows_begin;
     const bool read_back = accum && rr >= 0 && rr < n_rows;
-    const size_t rbase = ((size_t)(b * s.Hkv + kvh) * n_rows + (read_back ? rr : 0)) * D;
+    const size_t rbase = head_base(s, b, kvh, s.Hkv, n_rows) + (size_t)(read_back ? rr : 0) * ks;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const size_t idx = base + lane + 32 * t;
@@ -253,15 +256,17 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt_kernel(Shape s, const T*
   const int kvh = h / (s.Hq / s.Hkv);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * ROWS;
-  const size_t rowbase = (size_t)(b * s.Hq + h) * s.Sq;
-  const T* kh = k + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
-  const T* vh = v + (size_t)(b * s.Hkv + kvh) * s.Sk * D;
+  const size_t rowbase = (size_t)(b * s.Hq + h) * s.Sq;   // LSE and D rows
+  const size_t qs = row_stride(s, s.Hq), ks = row_stride(s, s.Hkv);   // row strides of one head
+  const size_t qbase = head_base(s, b, h, s.Hq, s.Sq);
+  const T* kh = k + head_base(s, b, kvh, s.Hkv, s.Sk);
+  const T* vh = v + head_base(s, b, kvh, s.Hkv, s.Sk);
 
   for (int idx = threadIdx.x; idx < ROWS * D; idx += kThreads) {
     const int r = idx / D, d = idx % D, i = row0 + r;
     const bool in = i < s.Sq;
-    Qs[r][d] = in ? to_f(q[(rowbase + i) * D + d]) : 0.f;
-    dOs[r][d] = in ? to_f(dO[(rowbase + i) * D + d]) : 0.f;
+    Qs[r][d] = in ? to_f(q[qbase + (size_t)i * qs + d]) : 0.f;
+    dOs[r][d] = in ? to_f(dO[qbase + (size_t)i * qs + d]) : 0.f;
   }
   float row_lse[RPW], row_d[RPW];
 #pragma unroll
@@ -287,8 +292,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt_kernel(Shape s, const T*
     for (int idx = threadIdx.x; idx < KT * D; idx += kThreads) {
       const int r = idx / D, d = idx % D, j = j0 + r;
       const bool in = j < s.Sk;
-      Ks[r][d] = in ? to_f(kh[(size_t)j * D + d]) : 0.f;
-      Vs[r][d] = in ? to_f(vh[(size_t)j * D + d]) : 0.f;
+      Ks[r][d] = in ? to_f(kh[(size_t)j * ks + d]) : 0.f;
+      Vs[r][d] = in ? to_f(vh[(size_t)j * ks + d]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt_kernel(Shape s, const T*
     const int i = row0 + warp * RPW + rr;
     if (i >= s.Sq) continue;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) from_f(dq + (rowbase + i) * D + lane + 32 * t, acc[rr][t] * s.scale);
+    for (int t = 0; t < NT; ++t) from_f(dq + qbase + (size_t)i * qs + lane + 32 * t, acc[rr][t] * s.scale);
   }
 }
 

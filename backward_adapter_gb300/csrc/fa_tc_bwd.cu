@@ -242,14 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       prefetch_tmap(&p.tm_q);
       prefetch_tmap(&p.tm_do);
       if (!C::RED_DQ) prefetch_tmap(&p.tm_dq);
-      const int kvrow = b * s.Hkv + kvh;
       if (!p.q8) {
         prefetch_tmap(&p.tm_k);
         prefetch_tmap(&p.tm_v);
         mbar_arrive_expect_tx(bar_kv, 2 * C::KV_TILE);
         for (int box = 0; box < D / 64; ++box) {
-          tma_load_3d(smem + C::OFF_K + box * C::KV_BOX, &p.tm_k, bar_kv, box * 64, j0, kvrow);
-          tma_load_3d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvrow);
+          tma_load_4d(smem + C::OFF_K + box * C::KV_BOX, &p.tm_k, bar_kv, box * 64, j0, kvh, b);
+          tma_load_4d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvh, b);
         }
       }
       uint32_t used_mask = 0, phase_mask = 0;
@@ -262,10 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (!mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101)) break;
         mbar_arrive_expect_tx(&bar_qdo_full[slot], 2 * C::Q_TILE);
         uint8_t* sq = smem + C::OFF_STAGE + slot * 2 * C::Q_TILE;
-        const int qrow = b * s.Hq + kvh * G + it.hh;
+        const int qh = kvh * G + it.hh;   // query head
         for (int box = 0; box < D / 64; ++box) {
-          tma_load_3d(sq + box * C::QBOX, &p.tm_q, &bar_qdo_full[slot], box * 64, it.i0, qrow);
-          tma_load_3d(sq + C::Q_TILE + box * C::QBOX, &p.tm_do, &bar_qdo_full[slot], box * 64, it.i0, qrow);
+          tma_load_4d(sq + box * C::QBOX, &p.tm_q, &bar_qdo_full[slot], box * 64, it.i0, qh, b);
+          tma_load_4d(sq + C::Q_TILE + box * C::QBOX, &p.tm_do, &bar_qdo_full[slot], box * 64, it.i0, qh, b);
         }
         used_mask |= 1u << slot;
         phase_mask = (phase_mask & ~(1u << slot)) | (ph << slot);
@@ -578,11 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (ok && st > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma_done, 0, abort_flag, p.status, 133));
     tc_fence_after();
     if (ok) {
-      const size_t row = ((size_t)(b * s.Hkv + kvh) * s.Sk + (key_ok ? j : 0)) * D;
+      const size_t row = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)(key_ok ? j : 0) * row_stride(s, s.Hkv);
       // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
       const long long rr = (long long)j - p.rows_begin;
       const bool read_back = p.accum && key_ok && rr >= 0 && rr < p.n_rows;
-      const size_t rrow = ((size_t)(b * s.Hkv + kvh) * p.n_rows + (read_back ? rr : 0)) * D;
+      const size_t rrow = head_base(s, b, kvh, s.Hkv, p.n_rows) + (size_t)(read_back ? rr : 0) * row_stride(s, s.Hkv);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float mul = which == 0 ? 1.f : s.scale;
@@ -796,8 +795,8 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   BwdTcParams p;
   memset(&p, 0, sizeof(p));
   cudaError_t e;
-  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_do, a.dO, s.Sq, s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&p.tm_q, a.q, s.layout, s.B, s.Hq, s.Sq, D, C::BQ)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&p.tm_do, a.dO, s.layout, s.B, s.Hq, s.Sq, D, C::BQ)) != cudaSuccess) return e;
   p.q8 = a.kq != nullptr ? 1 : 0;
   if (p.q8) {
     p.kq = a.kq;
@@ -805,8 +804,8 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.vq = a.vq;
     p.vd = static_cast<const __half*>(a.vd);
   } else {
-    if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
-    if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+    if ((e = make_tmap_4d(&p.tm_k, a.k, s.layout, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
+    if ((e = make_tmap_4d(&p.tm_v, a.v, s.layout, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
   }
   float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
   const int groups = dq_groups(s);

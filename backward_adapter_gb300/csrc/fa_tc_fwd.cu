@@ -174,11 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       mbar_arrive_expect_tx(bar_q, 2 * L::kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int box = 0; box < D / 64; ++box)
-          tma_load_3d(sQ + t * L::kTileBytes + box * L::kBoxBytes, &p.tm_q, bar_q, box * 64, q_row0 + t * kBM, bh);
+          tma_load_4d(sQ + t * L::kTileBytes + box * L::kBoxBytes, &p.tm_q, bar_q, box * 64, q_row0 + t * kBM, h, b);
       int slot = 0;
       uint32_t phase = 0;
       uint32_t used_mask = 0, phase_mask = 0;  // per slot: filled at least once / parity of its last fill
-      const int kvrow = b * s.Hkv + kvh;
       for (int j = kr.begin; j < kr.end; ++j) {
         if (skip_tile(p, mb, qt0, j)) continue;
         bool ok = true;
@@ -187,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           mbar_arrive_expect_tx(&bar_full[slot], L::kTileBytes);
           const CUtensorMap* map = which == 0 ? &p.tm_k : &p.tm_v;
           for (int box = 0; box < D / 64; ++box)
-            tma_load_3d(sKV + slot * L::kTileBytes + box * L::kBoxBytes, map, &bar_full[slot], box * 64, j * kBN,
-                        kvrow);
+            tma_load_4d(sKV + slot * L::kTileBytes + box * L::kBoxBytes, map, &bar_full[slot], box * 64, j * kBN,
+                        kvh, b);
           used_mask |= 1u << slot;
           phase_mask = (phase_mask & ~(1u << slot)) | (phase << slot);
           if (++slot == L::kSlots) { slot = 0; phase ^= 1; }
@@ -408,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const bool alive = l > 0.f;
       if (p.kv_splits == 1) {
         const float inv = alive ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + row * D);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + head_base(s, b, h, s.Hq, s.Sq) +
+                                              (size_t)(row_ok ? i : 0) * row_stride(s, s.Hq));
 #pragma unroll
         for (int cch = 0; cch < D / 32; ++cch) {
           uint32_t ov[32];
@@ -473,7 +473,7 @@ template <int D>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, int splits,
                                                           long long rows, __nv_bfloat16* __restrict__ o,
-                                                          float* __restrict__ lse) {
+                                                          float* __restrict__ lse, const Shape s) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -497,7 +497,9 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
   }
   const bool alive = l > 0.f;
   const float inv = alive ? 1.f / l : 0.f;
-  __nv_bfloat16* dst = o + row * D + lane * E;
+  const long long bh = row / s.Sq, i = row % s.Sq;   // rows run over [B, Hq, Sq] like LSE
+  __nv_bfloat16* dst = o + head_base(s, (int)(bh / s.Hq), (int)(bh % s.Hq), s.Hq, s.Sq) + (size_t)i * row_stride(s, s.Hq) +
+                       lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
   if (lane == 0) lse[row] = alive ? (mmax + __log2f(l)) * kLn2 : 0.f;
@@ -537,14 +539,17 @@ static EncodeTiledFn tensor_map_encoder() {
 }
 
 // bf16 [heads, S, D] tensor viewed as (D, S, heads), boxes of 64 x box_rows x 1 with 128-byte swizzle.
-cudaError_t make_tmap_bhsd(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
+cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int layout, int B, int H, int S, int D, int box_rows) {
   EncodeTiledFn encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t row = (cuuint64_t)D * 2, e = 2;
+  // byte strides of the S, H and B dimensions
+  const cuuint64_t strides[3] = {layout ? (cuuint64_t)H * D * e : row, layout ? row : (cuuint64_t)S * D * e,
+                                 (cuuint64_t)S * H * D * e};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -579,9 +584,10 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   const Shape& s = a.s;
   FwdTcParams p;
   cudaError_t e;
-  if ((e = make_tmap_bhsd(&p.tm_q, a.q, s.Sq, s.B * s.Hq, D, kBM)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_k, a.k, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
-  if ((e = make_tmap_bhsd(&p.tm_v, a.v, s.Sk, s.B * s.Hkv, D, kBN)) != cudaSuccess) return e;
+  const int kvl = a.kv_layout >= 0 ? a.kv_layout : s.layout;
+  if ((e = make_tmap_4d(&p.tm_q, a.q, s.layout, s.B, s.Hq, s.Sq, D, kBM)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&p.tm_k, a.k, kvl, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&p.tm_v, a.v, kvl, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + kBM - 1) / kBM;
@@ -610,7 +616,7 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   if (plan.kv_splits > 1) {
     const long long rows = (long long)s.B * s.Hq * s.Sq;
     fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(p.part_o, p.part_ml, plan.kv_splits,
-                                                                            rows, p.o, p.lse);
+                                                                            rows, p.o, p.lse, s);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

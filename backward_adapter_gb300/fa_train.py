@@ -21,6 +21,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA = r
 FA_F32, FA_BF16 = 0, 1
 FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
 FA_KV_DTYPE, FA_KV_Q8_0 = 0, 1
+FA_LAYOUT_BHSD, FA_LAYOUT_BSHD = 0, 1
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
@@ -35,7 +36,8 @@ class FaParams(ctypes.Structure):
                 ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("mask_kind", ctypes.c_int32), ("mask_batch", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("q_offset", ctypes.c_int64), ("deterministic", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+                ("q_offset", ctypes.c_int64), ("deterministic", ctypes.c_int32), ("kv_format", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class FaKvQ8(ctypes.Structure):
@@ -144,22 +146,30 @@ def _mask_view(mask: Optional[torch.Tensor]):
 def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] = None, *,
                 scale: Optional[float] = None, causal: bool = False,
                 q_offset: Optional[int] = None, window: int = 0, deterministic: bool = False,
-                kv_format: int = FA_KV_DTYPE) -> FaParams:
-    """Fill fa_params from tensor shapes. q: [B,Hq,Sq,D], k: [B,Hkv,Sk,D].
+                kv_format: int = FA_KV_DTYPE, layout: str = "bhsd") -> FaParams:
+    """Fill fa_params from tensor shapes. q: [B,Hq,Sq,D], k: [B,Hkv,Sk,D] (layout "bhsd"), or
+    q: [B,Sq,Hq,D], k: [B,Sk,Hkv,D] (layout "bshd": PyTorch's activations, no transpose copy).
 
     q_offset (causal or windowed) defaults to Sk - Sq: the query rows are the last Sq
     key positions. window is the sliding-window half-width (0 = none). deterministic makes
     the backward's dQ bitwise reproducible.
     """
-    B, Hq, Sq, D = q.shape
-    Hkv, Sk = k.shape[1], k.shape[2]
+    if layout == "bhsd":
+        B, Hq, Sq, D = q.shape
+        Hkv, Sk = k.shape[1], k.shape[2]
+    elif layout == "bshd":
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+    else:
+        raise ValueError(f"layout {layout!r}: 'bhsd' or 'bshd'")
     _, kind, mb = _mask_view(mask)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if q_offset is None:
         q_offset = Sk - Sq if (causal or window > 0) else 0
     return FaParams(B, Hq, Hkv, Sq, Sk, D, _dtype_code(q), float(scale), int(bool(causal)), kind, mb,
-                    int(window), int(q_offset), int(bool(deterministic)), int(kv_format))
+                    int(window), int(q_offset), int(bool(deterministic)), int(kv_format),
+                    FA_LAYOUT_BSHD if layout == "bshd" else FA_LAYOUT_BHSD, 0)
 
 
 def fwd_workspace_size(p: FaParams) -> int:
@@ -190,18 +200,18 @@ def _need_cuda(*ts):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
 
 
-def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, out=None, lse=None,
-        workspace=None, stream=None):
+def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, layout="bhsd",
+        out=None, lse=None, workspace=None, stream=None):
     """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic)
+                    deterministic=deterministic, layout=layout)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+        lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=q.device)
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(out), _ptr(lse),
@@ -209,14 +219,14 @@ def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0
     return out, lse
 
 
-def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk=None,
-        dv=None, workspace=None, stream=None):
+def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False,
+        layout="bhsd", dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic)
+                    deterministic=deterministic, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -228,8 +238,8 @@ def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=No
     return dq, dk, dv
 
 
-def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False,
-              dq=None, workspace=None, stream=None):
+def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, causal=False, q_offset=None, window=0,
+              deterministic=False, layout="bhsd", dq=None, workspace=None, stream=None):
     """Accumulating backward: dK/dV are added into fp32 dk_acc/dv_acc in place; returns dQ."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
@@ -237,7 +247,7 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic)
+                    deterministic=deterministic, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
@@ -248,12 +258,13 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
 
 
 def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows: int, mask=None, *, scale=None,
-                   causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk_rows=None, dv_rows=None, workspace=None,
-                   stream=None):
+                   causal=False, q_offset=None, window=0, deterministic=False, layout="bhsd", dq=None, dk_rows=None,
+                   dv_rows=None, workspace=None, stream=None):
     """Accumulating backward fused with the SET_ROWS backward of keys [rows_begin, rows_begin + n_rows).
 
     Adds dK/dV into dk_acc/dv_acc and also returns those keys' finished sums, read back in q's
-    dtype: (dQ, dK_rows [B, Hkv, n_rows, D], dV_rows [B, Hkv, n_rows, D]).
+    dtype: (dQ, dK_rows [B, Hkv, n_rows, D], dV_rows [B, Hkv, n_rows, D]), or [B, n_rows, Hkv, D]
+    with layout "bshd".
     """
     lib = load_library()
     mview, _, _ = _mask_view(mask)
@@ -261,9 +272,9 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic)
+                    deterministic=deterministic, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
-    shape = (k.shape[0], k.shape[1], int(n_rows), k.shape[3])
+    shape = (p.B, p.Hkv, int(n_rows), p.D) if layout == "bhsd" else (p.B, int(n_rows), p.Hkv, p.D)
     dk_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dk_rows is None else dk_rows
     dv_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dv_rows is None else dv_rows
     ws_bytes = bwd_workspace_size(p)
@@ -283,16 +294,22 @@ def _kv_q8(k_q, k_d, v_q, v_d) -> FaKvQ8:
     return FaKvQ8(k_q.data_ptr(), k_d.data_ptr(), v_q.data_ptr(), v_d.data_ptr())
 
 
-def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offset=None, window=0, out=None,
-           lse=None, workspace=None, stream=None):
+def _cache_shape_view(k_q, layout):
+    """The cache planes are [B, Hkv, Sk, ...] whatever the layout of Q: a view for the shapes only."""
+    return k_q if layout == "bhsd" else k_q.transpose(1, 2)
+
+
+def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offset=None, window=0, layout="bhsd",
+           out=None, lse=None, workspace=None, stream=None):
     """Forward over a q8_0 K/V cache (int8 values k_q/v_q, fp16 scales k_d/v_d per 32 features)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, mview)
     kv = _kv_q8(k_q, k_d, v_q, v_d)
-    p = make_params(q, k_q, mask, scale=scale, causal=causal, q_offset=q_offset, window=window, kv_format=FA_KV_Q8_0)
+    p = make_params(q, _cache_shape_view(k_q, layout), mask, scale=scale, causal=causal, q_offset=q_offset,
+                    window=window, kv_format=FA_KV_Q8_0, layout=layout)
     out = torch.empty_like(q) if out is None else out
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
+    lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=q.device) if lse is None else lse
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_fwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(out), _ptr(lse),
@@ -301,15 +318,16 @@ def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offs
 
 
 def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0,
-           deterministic=False, dq=None, dk=None, dv=None, dk_acc=None, dv_acc=None, workspace=None, stream=None):
+           deterministic=False, layout="bhsd", dq=None, dk=None, dv=None, dk_acc=None, dv_acc=None, workspace=None,
+           stream=None):
     """Backward over a q8_0 K/V cache. With dk_acc/dv_acc (fp32) the gradients of the dequantized
     K/V are added into them (returns dQ); otherwise returns (dQ, dK, dV) in q's dtype."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, o, lse, do, mview, dk_acc, dv_acc)
     kv = _kv_q8(k_q, k_d, v_q, v_d)
-    p = make_params(q, k_q, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, kv_format=FA_KV_Q8_0)
+    p = make_params(q, _cache_shape_view(k_q, layout), mask, scale=scale, causal=causal, q_offset=q_offset,
+                    window=window, deterministic=deterministic, kv_format=FA_KV_Q8_0, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
@@ -318,7 +336,7 @@ def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=F
                                          _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
                                          _stream(q.device, stream)))
         return dq
-    shape = tuple(k_q.shape)
+    shape = tuple(_cache_shape_view(k_q, layout).shape)   # dK / dV in the call's layout
     dk = torch.empty(shape, dtype=q.dtype, device=q.device) if dk is None else dk
     dv = torch.empty(shape, dtype=q.dtype, device=q.device) if dv is None else dv
     _check(lib.fa_train_bwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
@@ -373,8 +391,8 @@ def device_status() -> int:
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
-def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, dq=None, dk=None,
-                dv=None, stream=None):
+def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0,
+                deterministic=False, layout="bhsd", dq=None, dk=None, dv=None, stream=None):
     """Backward through fa_train_bwd_noalloc: no workspace is allocated or passed.
 
     For callers that cannot allocate device memory (their memory is owned by another
@@ -386,7 +404,7 @@ def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_o
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic)
+                    deterministic=deterministic, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -18,7 +18,8 @@
  *
  * Conventions (the pages leave these open; these are the plain readings):
  *   - Layout: every tensor is contiguous row-major. Q, O, dO, dQ: [B, Hq, Sq, D];
- *     K, V, dK, dV: [B, Hkv, Sk, D]; LSE: [B, Hq, Sq] fp32; mask: [mask_batch, Sq, Sk].
+ *     K, V, dK, dV: [B, Hkv, Sk, D] (or, with p->layout == FA_LAYOUT_BSHD, [B, Sq, Hq, D]
+ *     and [B, Sk, Hkv, D]); LSE: [B, Hq, Sq] fp32; mask: [mask_batch, Sq, Sk].
  *   - GQA: query head h reads key/value head h / (Hq / Hkv).
  *   - Additive mask (FA_MASK_ADD_F32): a value <= -1e9 (or -inf) hides the pair
  *     (its probability is exactly 0); any larger value is a bias added after scaling.
@@ -88,6 +89,12 @@ typedef enum fa_kv_format {
   FA_KV_Q8_0 = 1   /* K and V are a q8_0 cache (fa_kv_q8, the _q8 entry points) */
 } fa_kv_format;
 
+typedef enum fa_layout {
+  FA_LAYOUT_BHSD = 0, /* [B, H, S, D]: each head's rows contiguous */
+  FA_LAYOUT_BSHD = 1  /* [B, S, H, D]: each position's heads contiguous (PyTorch's [B, S, H, D]
+                         activations, no transpose copy); a row of one head is strided by H * D */
+} fa_layout;
+
 typedef struct fa_params {
   int32_t B;          /* batch, >= 1 */
   int32_t Hq;         /* query heads, a multiple of Hkv */
@@ -108,6 +115,10 @@ typedef struct fa_params {
                             Costs some backward speed and workspace. */
   int32_t kv_format;  /* fa_kv_format: FA_KV_DTYPE for the plain entry points, FA_KV_Q8_0 for the
                          _q8 ones (it sizes the workspace) */
+  int32_t layout;     /* fa_layout of Q, K, V, O, dO, dQ, dK, dV (and of dk_acc / dv_acc, dk_rows /
+                         dv_rows); LSE is always [B, Hq, Sq] and a q8_0 cache's planes always
+                         [B, Hkv, Sk, ...] */
+  int32_t reserved;   /* must be 0 */
 } fa_params;
 
 /* Bytes of scratch the forward needs for these parameters (0 when none). */

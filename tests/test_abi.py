@@ -48,15 +48,16 @@ def test_struct_layout_matches_header(tmp_path):
         pytest.skip("gcc not available")
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "fa_train.h"\n'
-                   'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(fa_params), offsetof(fa_params, scale),'
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(fa_params), offsetof(fa_params, scale),'
                    ' offsetof(fa_params, mask_batch), offsetof(fa_params, q_offset), offsetof(fa_params, deterministic),'
-                   ' offsetof(fa_params, kv_format), sizeof(fa_status));return 0;}\n')
+                   ' offsetof(fa_params, kv_format), offsetof(fa_params, layout), sizeof(fa_status));return 0;}\n')
     exe = tmp_path / "layout"
     subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     P = ft.FaParams
     assert [int(x) for x in got] == [ctypes.sizeof(P), P.scale.offset, P.mask_batch.offset, P.q_offset.offset,
-                                     P.deterministic.offset, P.kv_format.offset, ctypes.sizeof(ctypes.c_int)]
+                                     P.deterministic.offset, P.kv_format.offset, P.layout.offset,
+                                     ctypes.sizeof(ctypes.c_int)]
 
 
 def good_params(**kw):
@@ -82,6 +83,8 @@ BAD = [
     ("window_negative", dict(window=-1), ft.FA_ERR_INVALID_ARG),
     ("deterministic2", dict(deterministic=2), ft.FA_ERR_INVALID_ARG),
     ("kv_format", dict(kv_format=2), ft.FA_ERR_INVALID_ARG),
+    ("layout", dict(layout=2), ft.FA_ERR_INVALID_ARG),
+    ("reserved", dict(reserved=1), ft.FA_ERR_INVALID_ARG),
     ("window_offset_too_big", dict(window=8, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_too_big", dict(causal=1, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_negative", dict(causal=1, q_offset=-1), ft.FA_ERR_INVALID_ARG),
