@@ -217,6 +217,13 @@ BwdPlan plan_bwd(const Shape& s) {
       p.turn_bytes = (size_t)dq_groups(s) * s.B * s.Hq * ((s.Sq + 127) / 128) * 4;
       off = align_up(off + p.turn_bytes);
     }
+    static thread_local BwdSplit split;   // large; planned again at launch
+    plan_bwd_split(s, split);
+    if (split.n_units > 0) {
+      p.part_off = off;
+      p.part_bytes = (size_t)s.B * s.Hkv * split.n_slots * 2 * 128 * s.D * 4;
+      off = align_up(off + p.part_bytes);
+    }
   }
   p.total = off;
   return p;

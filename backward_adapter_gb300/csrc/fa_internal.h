@@ -92,6 +92,7 @@ struct BwdPlan {
   size_t dsum_off, dsum_bytes;   // fp32 [B, Hq, Sq]
   size_t dqacc_off, dqacc_bytes; // fp32 [groups, B, Hq, Sq, D]
   size_t turn_off, turn_bytes;   // deterministic: int32 [groups, B, Hq, ceil(Sq / 128)] dQ turn counters
+  size_t part_off, part_bytes;   // split key tiles: fp32 dK/dV partials [B * Hkv, slots, 2, 128, D]
   size_t total;
 };
 
@@ -117,6 +118,20 @@ void count_launches(int n);
 // sums the groups' accumulators in group order. Without it there is one accumulator.
 constexpr int kDetGroup = 8;
 inline int dq_groups(const Shape& s) { return s.deterministic ? ((s.Sk + 127) / 128 + kDetGroup - 1) / kDetGroup : 1; }
+
+// Backward work split (tensor-core path): a key tile whose query range is much longer than the
+// per-SM average share is split into up to kMaxParts parts, each a CTA of its own that writes fp32
+// dK/dV partials, summed afterwards in part order. Units run heaviest first.
+constexpr int kMaxUnits = 512;
+constexpr int kMaxParts = 8;
+struct BwdSplit {
+  int n_units = 0;        // 0: no split, one CTA per key tile in key-tile order
+  int n_slots = 0;        // partial slots per (batch, key/value head)
+  int n_split = 0;        // key tiles that are split
+  uint32_t units[kMaxUnits];   // kt | part << 12 | nparts << 16 | slot << 20, heaviest first
+  uint32_t split[kMaxUnits];   // kt | nparts << 12 | first slot << 16, for the partial sum
+};
+void plan_bwd_split(const Shape& s, BwdSplit& out);
 
 FwdPlan plan_fwd(const Shape& s);
 BwdPlan plan_bwd(const Shape& s);

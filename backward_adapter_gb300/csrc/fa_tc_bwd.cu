@@ -34,6 +34,8 @@
 // slot and added with one TMA bulk tensor reduce-add.
 #include <cuda.h>
 #include <cstring>
+#include <cmath>
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -122,7 +124,25 @@ struct BwdTcParams {
   __nv_bfloat16* dv_rows;
   int nqt, nkt;
   unsigned* status;
+  // work units (see BwdSplit): n_units == 0 runs one CTA per key tile in key-tile order
+  int n_units, n_slots;
+  float* part;                  // fp32 dK/dV partials of split key tiles [B * Hkv, n_slots, 2, 128, D]
+  uint32_t units[kMaxUnits];    // kt | part << 12 | nparts << 16 | slot << 20
 };
+
+// Query rows [ibeg, iend) that can see a key of tile kt, from the causal rule and the window, with
+// ibeg rounded down to a multiple of BQ (shared by the kernel and the host's work planner).
+__host__ __device__ inline void key_tile_rows(const Shape& s, int kt, int BQ, int& ibeg, int& iend) {
+  const int j0 = kt * kBN;
+  long long first = 0, last = (long long)s.Sq - 1;
+  if (s.causal) first = (long long)j0 - s.q_offset;
+  if (s.window > 0) {
+    if (!s.causal) first = (long long)j0 - s.q_offset - s.window;
+    last = min(last, (long long)j0 + kBN - 1 - s.q_offset + s.window);
+  }
+  ibeg = first <= 0 ? 0 : (int)min((first / BQ) * BQ, (long long)s.Sq);
+  iend = (int)max((long long)ibeg, last + 1);
+}
 
 // The steps of a CTA: (query head of the group, query tile) pairs in a fixed order; the tiles
 // run over the rows [ibeg, iend) that can see the CTA's keys. Head-major with ascending tiles by
@@ -189,21 +209,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   // ---- work unit: key tile kt of (b, kvh). Under the causal rule the low key tiles carry the most
   //      work, so blocks run key-tile-major: every head's heavy tiles are in the first wave and the
   //      light ones fill the SMs that free up (longest work first)
+  //      A split key tile's parts each take a consecutive share of its query tiles.
   const int nbkv = s.B * s.Hkv;
-  const int kt = blockIdx.x / nbkv;
+  int kt = blockIdx.x / nbkv, part = 0, nparts = 1, slot = 0;
+  if (p.n_units > 0) {
+    const uint32_t u = p.units[blockIdx.x / nbkv];
+    kt = (int)(u & 0xfffu);
+    part = (int)((u >> 12) & 0xfu);
+    nparts = (int)((u >> 16) & 0xfu);
+    slot = (int)(u >> 20);
+  }
   const int bkv = blockIdx.x % nbkv;
   const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
   const int j0 = kt * kBN;
   const int mb = s.mask_batch > 1 ? b : 0;
-  // query rows that can see a key of this tile: [first, last] from the causal rule and the window
-  long long first = 0, last = (long long)s.Sq - 1;
-  if (s.causal) first = (long long)j0 - s.q_offset;
-  if (s.window > 0) {
-    if (!s.causal) first = (long long)j0 - s.q_offset - s.window;
-    last = min(last, (long long)j0 + kBN - 1 - s.q_offset + s.window);
+  int ibeg, iend;
+  key_tile_rows(s, kt, BQ, ibeg, iend);
+  if (nparts > 1) {
+    const int tiles = (iend - ibeg + BQ - 1) / BQ;
+    const int t0 = part * tiles / nparts, t1 = (part + 1) * tiles / nparts;
+    const int base = ibeg;
+    ibeg = base + t0 * BQ;
+    iend = min(iend, base + t1 * BQ);
   }
-  const int ibeg = first <= 0 ? 0 : (int)min((first / BQ) * BQ, (long long)s.Sq);
-  const int iend = (int)max((long long)ibeg, last + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, p.q8 ? 8 : 1);   // q8: one arrival per softmax-grad warp after dequantizing
@@ -576,7 +604,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     ok = __all_sync(0xffffffffu, ok);
     if (ok && st > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma_done, 0, abort_flag, p.status, 133));
     tc_fence_after();
-    if (ok) {
+    if (ok && nparts > 1) {
+      // a part of a split key tile: its fp32 sums (dK scaled) go to the partial slot, summed later
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which == 0 ? 1.f : s.scale;
+        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
+        float* dst = p.part + ((((size_t)bkv * p.n_slots + slot) * 2 + which) * kBN + r) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = half * (D / 64) + cc;      // 32-feature chunk
+          uint32_t v[32];
+          if (st > 0) {
+            tmem_ld32(tcol + c * 32, v);
+            tmem_wait_ld();
+            reg_fence(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            d4[v4] = make_float4(__uint_as_float(v[4 * v4]) * mul, __uint_as_float(v[4 * v4 + 1]) * mul,
+                                 __uint_as_float(v[4 * v4 + 2]) * mul, __uint_as_float(v[4 * v4 + 3]) * mul);
+        }
+      }
+    } else if (ok) {
       const size_t row = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)(key_ok ? j : 0) * row_stride(s, s.Hkv);
       // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
       const long long rr = (long long)j - p.rows_begin;
@@ -784,9 +838,133 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
+// The parts of split key tiles, summed in part order: each thread takes 4 features of one key row,
+// for dK and dV, and writes them like the main kernel's epilogue would have.
+struct SplitReduceParams {
+  Shape s;
+  const float* part;
+  void* dk;
+  void* dv;
+  int accum;
+  long long rows_begin;
+  int n_rows;
+  __nv_bfloat16* dk_rows;
+  __nv_bfloat16* dv_rows;
+  int n_slots, n_split;
+  uint32_t split[kMaxUnits];   // kt | nparts << 12 | first slot << 16
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_split_reduce_kernel(const __grid_constant__ SplitReduceParams p) {
+  const Shape& s = p.s;
+  constexpr int V = D / 4;
+  const int nbkv = s.B * s.Hkv;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)p.n_split * nbkv * kBN * V) return;
+  const int c4 = (int)(idx % V);
+  const int r = (int)((idx / V) % kBN);
+  const long long rest = idx / ((long long)V * kBN);
+  const int bkv = (int)(rest % nbkv), si = (int)(rest / nbkv);
+  const uint32_t u = p.split[si];
+  const int kt = (int)(u & 0xfffu), np = (int)((u >> 12) & 0xfu), slot0 = (int)(u >> 16);
+  const int j = kt * kBN + r;
+  if (j >= s.Sk) return;
+  const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
+  const size_t out = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)j * row_stride(s, s.Hkv) + 4 * c4;
+  const long long rr = (long long)j - p.rows_begin;
+  const bool read_back = p.accum && rr >= 0 && rr < p.n_rows;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < np; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          p.part + ((((size_t)bkv * p.n_slots + slot0 + q) * 2 + which) * kBN + r) * D + 4 * c4);
+      a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    void* dst = which == 0 ? p.dv : p.dk;
+    if (p.accum) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + out);
+      float4 o = *d;
+      o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+      *d = o;
+      if (read_back) {
+        __nv_bfloat16* rows = which == 0 ? p.dv_rows : p.dk_rows;
+        *reinterpret_cast<uint2*>(rows + head_base(s, b, kvh, s.Hkv, p.n_rows) + (size_t)rr * row_stride(s, s.Hkv) +
+                                  4 * c4) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+      }
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst) + out) =
+          make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    }
+  }
+}
+
 }  // namespace
 
 bool tc_bwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq > 0; }
+
+void plan_bwd_split(const Shape& s, BwdSplit& out) {
+  out.n_units = out.n_slots = out.n_split = 0;
+  constexpr int kSms = 152;
+  constexpr int BQ = 128;   // the query tile of both configurations
+  const int nkt = (s.Sk + kBN - 1) / kBN, G = s.Hq / s.Hkv;
+  const long long nbkv = (long long)s.B * s.Hkv;
+  if (nkt > kMaxUnits || nkt > 4095) return;
+  // Only when one CTA per key tile leaves SMs idle: on a full GPU the heaviest-first key-tile order
+  // already balances the waves, and big parts pack worse. Never with deterministic dQ, whose turns
+  // need the key tiles dispatched in ascending order.
+  if (s.deterministic || (long long)nkt * nbkv >= kSms) return;
+  int tiles[kMaxUnits];
+  long long total = 0, heaviest = 0;
+  for (int kt = 0; kt < nkt; ++kt) {
+    int ib, ie;
+    key_tile_rows(s, kt, BQ, ib, ie);
+    tiles[kt] = ib < ie ? (ie - ib + BQ - 1) / BQ : 0;
+    total += (long long)G * tiles[kt];
+    heaviest = std::max(heaviest, (long long)G * tiles[kt]);
+  }
+  // the per-SM share of all steps; a key tile well above it is split into parts of about that size
+  const double share = (double)(total * nbkv) / kSms;
+  if (share <= 0 || heaviest <= share) return;
+  int nparts[kMaxUnits];
+  int units = 0, split = 0;
+  for (int kt = 0; kt < nkt; ++kt) {
+    const long long steps = (long long)G * tiles[kt];
+    int np = 1;
+    // parts of at least 4 steps: shorter CTAs spend most of their time filling and draining
+    if (steps > share)
+      np = (int)std::min<long long>({kMaxParts, tiles[kt], steps / 4, (long long)std::ceil(steps / share)});
+    nparts[kt] = std::max(1, np);
+    units += nparts[kt];
+    split += nparts[kt] > 1;
+  }
+  if (split == 0 || units > kMaxUnits) return;
+  // slots of the split tiles' parts, then the units sorted heaviest first (ties in key-tile order)
+  int slot_of[kMaxUnits];
+  int slots = 0;
+  for (int kt = 0; kt < nkt; ++kt) {
+    slot_of[kt] = slots;
+    if (nparts[kt] > 1) {
+      out.split[out.n_split++] = (uint32_t)kt | (uint32_t)nparts[kt] << 12 | (uint32_t)slots << 16;
+      slots += nparts[kt];
+    }
+  }
+  if (slots >= 4096) return;
+  struct U { double work; int kt, part; };
+  U list[kMaxUnits];
+  int n = 0;
+  for (int kt = 0; kt < nkt; ++kt)
+    for (int q = 0; q < nparts[kt]; ++q)
+      list[n++] = U{(double)G * tiles[kt] / nparts[kt], kt, q};
+  std::stable_sort(list, list + n, [](const U& a, const U& b) { return a.work > b.work; });
+  for (int i = 0; i < n; ++i) {
+    const int kt = list[i].kt, q = list[i].part;
+    const uint32_t slot = nparts[kt] > 1 ? (uint32_t)(slot_of[kt] + q) : 0u;
+    out.units[i] = (uint32_t)kt | (uint32_t)q << 12 | (uint32_t)nparts[kt] << 16 | slot << 20;
+  }
+  out.n_units = n;
+  out.n_slots = slots;
+}
 
 template <int D>
 static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, unsigned* status) {
@@ -838,15 +1016,41 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.turn = reinterpret_cast<int*>(ws + plan.turn_off);
     if ((e = cudaMemsetAsync(p.turn, 0, plan.turn_bytes, a.stream)) != cudaSuccess) return e;
   }
+  static thread_local BwdSplit split;
+  plan_bwd_split(s, split);
+  p.n_units = split.n_units;
+  p.n_slots = split.n_slots;
+  p.part = split.n_units > 0 ? reinterpret_cast<float*>(ws + plan.part_off) : nullptr;
+  memcpy(p.units, split.units, sizeof(uint32_t) * split.n_units);
   const int smem = C::BYTES;
   if ((e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
-  const long long ctas = (long long)s.B * s.Hkv * p.nkt;
+  const long long ctas = (long long)s.B * s.Hkv * (split.n_units > 0 ? split.n_units : p.nkt);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if ((e = prof_begin(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
   bwd_tc_kernel<D><<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (split.n_units > 0) {
+    // the split key tiles' parts, summed in part order into dK / dV
+    static thread_local SplitReduceParams r;
+    r.s = s;
+    r.part = p.part;
+    r.dk = a.dk;
+    r.dv = a.dv;
+    r.accum = p.accum;
+    r.rows_begin = p.rows_begin;
+    r.n_rows = p.n_rows;
+    r.dk_rows = p.dk_rows;
+    r.dv_rows = p.dv_rows;
+    r.n_slots = split.n_slots;
+    r.n_split = split.n_split;
+    memcpy(r.split, split.split, sizeof(uint32_t) * split.n_split);
+    const long long threads = (long long)split.n_split * s.B * s.Hkv * kBN * (D / 4);
+    bwd_split_reduce_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(r);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if ((e = prof_end(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
   return launch_dq_convert(a, dq_acc, groups);
 }
