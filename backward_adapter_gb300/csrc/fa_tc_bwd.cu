@@ -26,7 +26,8 @@
 // warp writes TMEM another warp still reads.
 //
 // Each step's softmax-grad is split in two rounds of 64 queries; the first round's
-// dV / dK MMAs run while the second round is computed.
+// dV / dK MMAs run while the second round is computed. S^T and dP^T complete on separate
+// barriers, so the first round's exponentials run under the dP^T MMAs.
 // D = 128: the dQ^T partial goes from TMEM to registers and into the accumulator with
 // coalesced red.add (one 128-byte run of 32 features per warp instruction), so it
 // needs no shared memory, and the Q/dO slot is handed back by the MMA commit after
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // NDS: the dQ MMA has read that dS^T buffer
   uint64_t* bar_mma_done = bar_ds_free + C::NDS;        // 1
   uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 4 stager warps filled the dQ staging
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_stage_full + 1);
+  uint64_t* bar_s_full = bar_stage_full + 1;            // NBUF: S^T of the block is in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s_full + C::NBUF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* lsed = reinterpret_cast<float*>(smem + C::OFF_LSED);
 
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&bar_sdp_full[i], 1);
+      mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_p_full[i], 8);
       mbar_init(&bar_dq_full[i], 1);
       mbar_init(&bar_dq_free[i], 4);
@@ -261,6 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   auto step_skipped = [&](const StepIter& it) { return bwd_tile_code(p, mb, it.i0, kt) == TILE_SKIP; };
+  auto count_steps = [&]() {
+    int n = 0;
+    StepIter it;
+    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    for (; it.valid(); it.next())
+      if (!step_skipped(it)) ++n;
+    return n;
+  };
 
   if (warp < 4) {
    regs_dec<kRegsControl>();   // all four warps of the control warpgroup
@@ -329,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         for (int k = 0; k < D / 16; ++k)
           mma_ss(tb, desc_add(dK0, (k / 4) * C::KV_BOX + (k % 4) * 32), desc_add(dq0, (k / 4) * C::QBOX + (k % 4) * 32),
                  idesc_s, k > 0);
+        mma_commit(&bar_s_full[st % C::NBUF]);   // the softmax-grad warps start on P^T under dP^T
       };
       // dP^T of step st: its TMEM block held the dQ partial of step st - NBUF, drained by the stager
       auto issue_dp = [&](int st) {
@@ -389,13 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       //   S^T of step nt: after its Q / dO are loaded and step nt-1 was issued completely.
       // The issue order of the groups that accumulate (dV, dK) is fixed, so they are bitwise
       // reproducible.
-      int total = 0;
-      {
-        StepIter it;
-        it.init(G, iend, BQ, ibeg, s.deterministic != 0);
-        for (; it.valid(); it.next())
-          if (!step_skipped(it)) ++total;
-      }
+      const int total = count_steps();
       int nt = 0, np = 0, ns = 0, na = 0;   // na: steps whose first-half dV/dK are issued
       unsigned long long idle_since = globaltimer();
       while (ok && ns < total) {
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
       const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st % C::NDS;
-      ok = mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
+      ok = mbar_wait(&bar_s_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
       if (st >= C::NDS) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - C::NDS) / C::NDS) & 1, abort_flag, p.status, 132);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
@@ -507,29 +513,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // round cc covers queries [64cc, 64cc + 64): the two warps of a lane quadrant take one
         // 32-query chunk each, and the first round is handed to the dV / dK MMAs right away
         const int c = cc * 2 + half;   // score chunk: queries [32c, 32c+32)
-        // the chunk's scores and dP^T in one go (one TMEM round trip; the score columns then
-        // receive P^T and dS^T), LSE / D 16 queries at a time
+        // P^T of the chunk from its scores: in the first round while the dP^T MMAs still run, in
+        // the second with dP^T loaded in the same TMEM round trip; the score columns then
+        // receive P^T and dS^T
         uint32_t sr[32], dr[32];
         tmem_ld32(tb + c * 32, sr);
-        tmem_ld32(tb + BQ + c * 32, dr);
+        if (cc > 0) tmem_ld32(tb + BQ + c * 32, dr);
         tmem_wait_ld();
         reg_fence(sr);
-        reg_fence(dr);
+        float pv[32];
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           const int q0 = c * 32 + sub * 16;   // first query of these 16
-          float l2[16], dv_[16];
+          float l2[16];
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             const float4 a = ld_shared_f4(lse_s + (q0 + 4 * v4) * 4);
-            const float4 d = ld_shared_f4(lse_s + (BQ + q0 + 4 * v4) * 4);
             l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
-            dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
           }
-          float pv[16];
+          float* pw = pv + sub * 16;
           if (full) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) pv[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
+            for (int e = 0; e < 16; ++e) pw[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
           } else {
             // visible query rows of this key are [rlo, rhi) relative to base (causal rule, window,
             // query tail); rhi <= rlo when none is
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (code != TILE_MIXED) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                pv[e] = (e >= rlo && e < rhi) ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e])) : 0.f;
+                pw[e] = (e >= rlo && e < rhi) ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e])) : 0.f;
             } else {
               // the 16 mask values of this key (one per query row) first, then the arithmetic
               float bias[16];
@@ -558,21 +563,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
               }
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                pv[e] = bias[e] != -CUDART_INF_F
+                pw[e] = bias[e] != -CUDART_INF_F
                             ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias[e] - l2[e]))
                             : 0.f;
             }
           }
-          uint32_t pk[8], dk8[8];
+          uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-            dk8[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(dr[sub * 16 + 2 * e]) - dv_[2 * e]),
-                                 pv[2 * e + 1] * (__uint_as_float(dr[sub * 16 + 2 * e + 1]) - dv_[2 * e + 1]));
+          for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(pw[2 * e], pw[2 * e + 1]);
+          tmem_st8(tb + c * 32 + sub * 8, pk);   // P^T of these 16 queries
+        }
+        if (cc == 0) {
+          // dP^T of the step (its MMAs ran under the exponentials above)
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 135));
+          if (!ok) break;
+          tc_fence_after();
+          tmem_ld32(tb + BQ + c * 32, dr);
+          tmem_wait_ld();
+        }
+        reg_fence(dr);
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int q0 = c * 32 + sub * 16;
+          float dv_[16];
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const float4 d = ld_shared_f4(lse_s + (BQ + q0 + 4 * v4) * 4);
+            dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
           }
-          // P^T and dS^T of these 16 queries over this chunk's own (already read) score columns
-          tmem_st8(tb + c * 32 + sub * 8, pk);
-          tmem_st8(tb + c * 32 + 16 + sub * 8, dk8);
+          const float* pw = pv + sub * 16;
+          uint32_t dk8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dk8[e] = pack_bf16x2(pw[2 * e] * (__uint_as_float(dr[sub * 16 + 2 * e]) - dv_[2 * e]),
+                                 pw[2 * e + 1] * (__uint_as_float(dr[sub * 16 + 2 * e + 1]) - dv_[2 * e + 1]));
+          tmem_st8(tb + c * 32 + 16 + sub * 8, dk8);   // dS^T of these 16 queries
           // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (2 x 16 B chunks)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -588,6 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_p_half);
         }
+      }
+      if (!ok) {
+        tmem_wait_st();
+        break;
       }
       tmem_wait_st();
       fence_proxy_async_smem();
