@@ -158,14 +158,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, x: float) -> float:
+def max_over_ranks(world, x: float, device: str = "cuda") -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, rank_ms: float, device: str = "cuda"):
+    """Replicas: (slowest rank's ms per step, every rank's work over that time in TFLOP/s)."""
+    ms = max_over_ranks(world, rank_ms, device)
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 # ---------------------------------------------------------------------------------------------
@@ -359,8 +365,7 @@ def run_ours(args):
             return 0.0
 
     kern_ms = {kid: mean_or_zero(evs) for kid, evs in kern.items()}
-    mean_ms = max_over_ranks(world, statistics.mean(step_ms))
-    value = world * fl["total"] / (mean_ms * 1e-3) / 1e12
+    mean_ms, value = job_tflops(world, fl["total"], statistics.mean(step_ms))
 
     peaks = load_peaks()
     fwd_ms, bwd_main_ms = kern_ms[ft.FA_KERNEL_FWD], kern_ms[ft.FA_KERNEL_BWD_MAIN]
@@ -429,8 +434,7 @@ def run_ours(args):
     e1.record(comp)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / E)
-    e2e_value = world * fl["total"] / (e2e_ms * 1e-3) / 1e12
+    e2e_ms, e2e_value = job_tflops(world, fl["total"], e0.elapsed_time(e1) / E)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
