@@ -54,8 +54,11 @@ fa_status check_params(const fa_params* p, Shape& s) {
   if (p->deterministic != 0 && p->deterministic != 1) {
     set_error("deterministic=%d must be 0 or 1", p->deterministic); return FA_ERR_INVALID_ARG;
   }
-  if (p->kv_format != FA_KV_DTYPE && p->kv_format != FA_KV_Q8_0) {
+  if (p->kv_format != FA_KV_DTYPE && p->kv_format != FA_KV_Q8_0 && p->kv_format != FA_KV_F16) {
     set_error("kv_format=%d invalid", p->kv_format); return FA_ERR_INVALID_ARG;
+  }
+  if (p->kv_format == FA_KV_F16 && p->dtype != FA_BF16) {
+    set_error("an f16 K/V cache needs bf16 queries (dtype=%d)", p->dtype); return FA_ERR_UNSUPPORTED;
   }
   if (p->layout != FA_LAYOUT_BHSD && p->layout != FA_LAYOUT_BSHD) {
     set_error("layout=%d invalid", p->layout); return FA_ERR_INVALID_ARG;
@@ -75,7 +78,7 @@ fa_status check_params(const fa_params* p, Shape& s) {
   s.window = (p->window > 0 && p->window < p->Sk) ? p->window : 0;
   s.q_offset = (p->causal || s.window > 0) ? (long long)p->q_offset : 0;
   s.deterministic = p->deterministic;
-  s.kv_q8 = p->kv_format == FA_KV_Q8_0 ? 1 : 0;
+  s.kv_format = p->kv_format;
   s.layout = p->layout;
   return FA_OK;
 }
@@ -175,8 +178,8 @@ FwdPlan plan_fwd(const Shape& s) {
     p.tilemap_bytes = (size_t)s.mask_batch * ((s.Sq + 127) / 128) * ((s.Sk + 127) / 128);
     off = align_up(off + p.tilemap_bytes);
   }
-  if (p.tensor_core && s.kv_q8) {
-    // the q8_0 cache dequantized to bf16 K then V (read by every query tile of the forward)
+  if (p.tensor_core && s.kv_format != FA_KV_DTYPE) {
+    // the q8_0 or f16 cache as bf16 K then V (read by every query tile of the forward)
     p.kvbf_off = off;
     p.kvbf_bytes = 2 * (size_t)s.B * s.Hkv * s.Sk * s.D * 2;
     off = align_up(off + p.kvbf_bytes);
@@ -224,6 +227,11 @@ BwdPlan plan_bwd(const Shape& s) {
       p.part_bytes = (size_t)s.B * s.Hkv * split.n_slots * 2 * 128 * s.D * 4;
       off = align_up(off + p.part_bytes);
     }
+    if (s.kv_format == FA_KV_F16) {
+      p.kvbf_off = off;
+      p.kvbf_bytes = 2 * (size_t)s.B * s.Hkv * s.Sk * s.D * 2;
+      off = align_up(off + p.kvbf_bytes);
+    }
   }
   p.total = off;
   return p;
@@ -247,7 +255,7 @@ size_t fa_train_bwd_workspace_size(const fa_params* p) {
   return plan_bwd(s).total;
 }
 
-// The K/V inputs of a call: tensors in the params' dtype, or a q8_0 cache (value and scale planes).
+// The K/V inputs of a call: tensors in the params' dtype or fp16, or a q8_0 cache (value and scale planes).
 struct KvIn {
   const void* k;
   const void* v;
@@ -256,12 +264,13 @@ struct KvIn {
 
 // Appends the K/V input spans to `in` (2 for tensors, 4 for a q8_0 cache).
 static fa_status kv_spans(const Shape& s, const KvIn& kv, Span* in, int& n) {
-  if ((kv.q8 != nullptr) != (s.kv_q8 != 0)) {
-    set_error(s.kv_q8 ? "kv_format is FA_KV_Q8_0: use the _q8 entry points" : "the _q8 entry points need kv_format FA_KV_Q8_0");
+  const bool q8 = s.kv_format == FA_KV_Q8_0;
+  if ((kv.q8 != nullptr) != q8) {
+    set_error(q8 ? "kv_format is FA_KV_Q8_0: use the _q8 entry points" : "the _q8 entry points need kv_format FA_KV_Q8_0");
     return FA_ERR_INVALID_ARG;
   }
   if (kv.q8 == nullptr) {
-    const size_t es = elem_size(s);
+    const size_t es = s.kv_format == FA_KV_F16 ? 2 : elem_size(s);
     in[n++] = {kv.k, kv_bytes(s, es), "k"};
     in[n++] = {kv.v, kv_bytes(s, es), "v"};
     return FA_OK;
@@ -294,10 +303,23 @@ static fa_status fwd_common(const fa_params* p, const void* q, const KvIn& kv, c
   all[nin + 1] = out[1];
   if ((st = check_ws(ws, ws_bytes, plan.total, all, nin + 2)) != FA_OK) return st;
   if (s.Sq == 0) return FA_OK;
-  if (kv.q8 != nullptr && !plan.tensor_core) { set_error("a q8_0 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED; }
+  if (s.kv_format != FA_KV_DTYPE && !plan.tensor_core) {
+    set_error("a quantized or f16 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED;
+  }
 
   FwdArgs a{s, q, kv.k, kv.v, mask, o, lse, (cudaStream_t)stream};
   cudaError_t e = cudaSuccess;
+  if (s.kv_format == FA_KV_F16) {
+    // the tensor cores multiply bf16 by bf16: round the cache to a bf16 copy in the call's layout
+    char* kbf = (char*)ws + plan.kvbf_off;
+    char* vbf = kbf + plan.kvbf_bytes / 2;
+    const long long n = (long long)s.B * s.Hkv * s.Sk * s.D;
+    e = launch_f16_to_bf16(kv.k, kbf, n, a.stream);
+    if (e == cudaSuccess) e = launch_f16_to_bf16(kv.v, vbf, n, a.stream);
+    if (e != cudaSuccess) return cuda_status(e, "f16 cache cast launch");
+    a.k = kbf;
+    a.v = vbf;
+  }
   if (kv.q8 != nullptr) {
     // every query tile reads every key tile: dequantize the cache once, then run the bf16 kernel on it
     char* kbf = (char*)ws + plan.kvbf_off;
@@ -378,8 +400,20 @@ static fa_status bwd_common(const fa_params* p, const void* q, const KvIn& kv, c
     if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, gk, cs);
     return cuda_status(e, "zero dK/dV");
   }
-  if (kv.q8 != nullptr && !plan.tensor_core) { set_error("a q8_0 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED; }
+  if (s.kv_format != FA_KV_DTYPE && !plan.tensor_core) {
+    set_error("a quantized or f16 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED;
+  }
   BwdArgs a{s, q, kv.k, kv.v, mask, o, lse, dO, dq, dk, dv, accum, cs};
+  if (s.kv_format == FA_KV_F16) {
+    char* kbf = (char*)ws + plan.kvbf_off;
+    char* vbf = kbf + plan.kvbf_bytes / 2;
+    const long long n = (long long)s.B * s.Hkv * s.Sk * s.D;
+    cudaError_t e = launch_f16_to_bf16(kv.k, kbf, n, cs);
+    if (e == cudaSuccess) e = launch_f16_to_bf16(kv.v, vbf, n, cs);
+    if (e != cudaSuccess) return cuda_status(e, "f16 cache cast launch");
+    a.k = kbf;
+    a.v = vbf;
+  }
   if (kv.q8 != nullptr) {
     a.kq = kv.q8->k_q;
     a.kd = kv.q8->k_d;

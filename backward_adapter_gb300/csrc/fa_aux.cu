@@ -261,3 +261,38 @@ cudaError_t launch_q8_dequant(const Shape& s, const int8_t* xq, const void* xd, 
 }
 
 }  // namespace fa
+
+namespace fa {
+namespace {
+
+// One thread per 8 elements: one 16-byte load of fp16, one 16-byte store of bf16 (each value
+// widened exactly to fp32, then rounded to nearest even).
+__global__ void __launch_bounds__(256) f16_to_bf16_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
+                                                          long long segs) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= segs) return;
+  const uint4 raw = __ldg(x + i);
+  const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&in[k]));
+    w[k] = tc::pack_bf16x2(f.x, f.y);
+  }
+  out[i] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_f16_to_bf16(const void* x, void* out, long long n, cudaStream_t st) {
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const long long segs = n / 8;
+  if (segs == 0) return cudaSuccess;
+  const long long blocks = (segs + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  f16_to_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(x), static_cast<uint4*>(out), segs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -23,7 +23,7 @@ struct Shape {
   int window;          // sliding-window half-width, 0 = none
   long long q_offset;  // key position of query row 0 (0 unless causal or windowed)
   int deterministic;   // the backward adds dQ partials in a fixed order
-  int kv_q8;           // K/V come from a q8_0 cache
+  int kv_format;       // fa_kv_format of the call (read by the host side only)
   int layout;          // 0: [B, H, S, D]; 1: [B, S, H, D] (Q, K, V, O, dO, dQ, dK, dV)
 };
 
@@ -82,7 +82,7 @@ struct FwdPlan {
   size_t tilemap_off, tilemap_bytes;
   size_t part_o_off, part_o_bytes;     // fp32 [splits, B, Hq, Sq, D]
   size_t part_ml_off, part_ml_bytes;   // fp32 [splits, B, Hq, Sq, 2]
-  size_t kvbf_off, kvbf_bytes;         // q8_0 cache: bf16 K then V [B, Hkv, Sk, D]
+  size_t kvbf_off, kvbf_bytes;         // q8_0 or f16 cache: bf16 K then V (q8_0: [B, Hkv, Sk, D]; f16: the layout)
   size_t total;
 };
 
@@ -93,6 +93,7 @@ struct BwdPlan {
   size_t dqacc_off, dqacc_bytes; // fp32 [groups, B, Hq, Sq, D]
   size_t turn_off, turn_bytes;   // deterministic: int32 [groups, B, Hq, ceil(Sq / 128)] dQ turn counters
   size_t part_off, part_bytes;   // split key tiles: fp32 dK/dV partials [B * Hkv, slots, 2, 128, D]
+  size_t kvbf_off, kvbf_bytes;   // f16 cache: bf16 K then V, in the call's layout
   size_t total;
 };
 
@@ -149,6 +150,8 @@ cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tile
 
 // q8_0 cache -> bf16 [B, Hkv, Sk, D] (x = scale[d / 32] * q[d], rounded to nearest even).
 cudaError_t launch_q8_dequant(const Shape& s, const int8_t* xq, const void* xd, void* out, cudaStream_t st);
+// fp16 -> bf16, n elements (a multiple of 8; 16-byte aligned buffers), rounded to nearest even.
+cudaError_t launch_f16_to_bf16(const void* x, void* out, long long n, cudaStream_t st);
 
 // SET_ROWS backward gather (fa_set_rows_backward): out[bh, r, :] = acc[bh, idx[r], :].
 constexpr unsigned kSiteRowIndex = 950;

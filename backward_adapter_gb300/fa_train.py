@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libfa_train.so")
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA = range(5)
 FA_F32, FA_BF16 = 0, 1
 FA_MASK_NONE, FA_MASK_ADD_F32, FA_MASK_BOOL_U8 = 0, 1, 2
-FA_KV_DTYPE, FA_KV_Q8_0 = 0, 1
+FA_KV_DTYPE, FA_KV_Q8_0, FA_KV_F16 = 0, 1, 2
 FA_LAYOUT_BHSD, FA_LAYOUT_BSHD = 0, 1
 
 EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_train_fwd", "fa_train_bwd",
@@ -143,6 +143,17 @@ def _mask_view(mask: Optional[torch.Tensor]):
     raise TypeError(f"mask dtype {mask.dtype}: float32 (additive) or uint8/bool (1 = attend)")
 
 
+def _kv_format(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """K/V in q's dtype, or an fp16 cache under bf16 queries (rounded to bf16 by the library)."""
+    if k.dtype != v.dtype:
+        raise TypeError(f"k ({k.dtype}) and v ({v.dtype}) must have one dtype")
+    if k.dtype == q.dtype:
+        return FA_KV_DTYPE
+    if k.dtype == torch.float16 and q.dtype == torch.bfloat16:
+        return FA_KV_F16
+    raise TypeError(f"k/v dtype {k.dtype} with q dtype {q.dtype}: same as q, or float16 under bfloat16 q")
+
+
 def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] = None, *,
                 scale: Optional[float] = None, causal: bool = False,
                 q_offset: Optional[int] = None, window: int = 0, deterministic: bool = False,
@@ -202,12 +213,13 @@ def _need_cuda(*ts):
 
 def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, layout="bhsd",
         out=None, lse=None, workspace=None, stream=None):
-    """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32)."""
+    """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32). k and v are in q's dtype,
+    or float16 (an fp16 cache) under bfloat16 q."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, layout=layout)
+                    deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -221,15 +233,15 @@ def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0
 
 def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False,
         layout="bhsd", dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers)."""
+    """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers); k and v as in fwd."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, layout=layout)
+                    deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dk = torch.empty_like(k, dtype=q.dtype) if dk is None else dk   # q's dtype for an fp16 cache too
+    dv = torch.empty_like(v, dtype=q.dtype) if dv is None else dv
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
@@ -247,7 +259,7 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, layout=layout)
+                    deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
@@ -272,7 +284,7 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, layout=layout)
+                    deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     shape = (p.B, p.Hkv, int(n_rows), p.D) if layout == "bhsd" else (p.B, int(n_rows), p.Hkv, p.D)
     dk_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dk_rows is None else dk_rows
@@ -404,10 +416,10 @@ def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_o
     mview, _, _ = _mask_view(mask)
     _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
-                    deterministic=deterministic, layout=layout)
+                    deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dk = torch.empty_like(k, dtype=q.dtype) if dk is None else dk   # q's dtype for an fp16 cache too
+    dv = torch.empty_like(v, dtype=q.dtype) if dv is None else dv
     _check(lib.fa_train_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
                                     _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(q.device, stream)))
     return dq, dk, dv

@@ -44,7 +44,8 @@ class Workload:
     causal: bool = False
     q_offset: int = 0            # query row i sits at key position q_offset + i
     window: int = 0              # sliding window half-width (0 = none)
-    kv_format: str = "bf16"      # "bf16" (K/V in dtype) or "q8_0" (8-bit values + fp16 scale per 32 features)
+    kv_format: str = "bf16"      # "bf16" (K/V in dtype), "q8_0" (8-bit values + fp16 scale per 32 features)
+    #                              or "f16" (an fp16 K/V cache under bf16 Q / dO)
     mask: str = "none"           # none | extra_row | pad_self | cross | random_bool | random_add
     accum: bool = False          # dK/dV accumulate into prefilled fp32 buffers
     do_std: float = 1.0          # standard deviation of dO
@@ -80,8 +81,10 @@ DIT_SELF_WINDOW = Workload("dit_self_window128_gqa_pad_s1024_d64", B=1, Hq=16, H
 
 # The long-window chunk over a q8_0 K/V cache read in place (the cache format the walk trains in).
 LONG_WINDOW_Q8 = LONG_WINDOW.with_(name="chunk512_window67584_h16_kv4_d128_accum_q8cache", kv_format="q8_0")
+# The same chunk over an fp16 cache (the other cache type the walk reads in place).
+LONG_WINDOW_F16 = LONG_WINDOW.with_(name="chunk512_window67584_h16_kv4_d128_accum_f16cache", kv_format="f16")
 
-BY_NAME = {w.name: w for w in WORKLOADS + [DIT_SELF_WINDOW, LONG_WINDOW_Q8]}
+BY_NAME = {w.name: w for w in WORKLOADS + [DIT_SELF_WINDOW, LONG_WINDOW_Q8, LONG_WINDOW_F16]}
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -169,8 +172,12 @@ def make_inputs(w: Workload) -> dict:
     k = _normal(rng, (w.B, w.Hkv, w.Sk, w.D), 1.0)
     v = _normal(rng, (w.B, w.Hkv, w.Sk, w.D), 1.0)
     do = _normal(rng, (w.B, w.Hq, w.Sq, w.D), w.do_std)
+    if w.kv_format == "f16":   # the cache holds fp16 values (finer than bf16: the cast is exercised)
+        k, v = (t.astype(np.float16).astype(np.float32) for t in (k, v))
     if w.dtype == "bf16":
-        q, k, v, do = (round_to_bf16(t) for t in (q, k, v, do))
+        q, do = round_to_bf16(q), round_to_bf16(do)
+        if w.kv_format != "f16":
+            k, v = round_to_bf16(k), round_to_bf16(v)
     out = {"q": q, "k": k, "v": v, "do": do}
     if w.kv_format == "q8_0":
         out["k_q8"] = quantize_q8_0(k)

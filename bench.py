@@ -263,6 +263,9 @@ def run_ours(args):
 
     q8 = w.kv_format == "q8_0"
     host = {n: torch.from_numpy(inputs[n]).to(dt).pin_memory() for n in (("q", "do") if q8 else ("q", "k", "v", "do"))}
+    if w.kv_format == "f16":   # an fp16 K/V cache, read in place (the library casts it for the tensor cores)
+        for n in ("k", "v"):
+            host[n] = torch.from_numpy(inputs[n]).to(torch.float16).pin_memory()
     if q8:   # the K/V cache in its own format: int8 values and fp16 scales, read in place
         for n in ("k", "v"):
             qv, dv_ = inputs[n + "_q8"]
@@ -273,7 +276,8 @@ def run_ours(args):
     d = {n: t.to(dev) for n, t in host.items()}
     mask = d.get("mask")
     kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=args.deterministic)
-    p = ft.make_params(d["q"], d["k_q" if q8 else "k"], mask, **kw)
+    kv_format = {"q8_0": ft.FA_KV_Q8_0, "f16": ft.FA_KV_F16}.get(w.kv_format, ft.FA_KV_DTYPE)
+    p = ft.make_params(d["q"], d["k_q" if q8 else "k"], mask, kv_format=kv_format, **kw)
     ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
     o = torch.empty_like(d["q"])

@@ -86,7 +86,15 @@ typedef enum fa_mask_kind {
 
 typedef enum fa_kv_format {
   FA_KV_DTYPE = 0, /* K and V are tensors in p->dtype */
-  FA_KV_Q8_0 = 1   /* K and V are a q8_0 cache (fa_kv_q8, the _q8 entry points) */
+  FA_KV_Q8_0 = 1,  /* K and V are a q8_0 cache (fa_kv_q8, the _q8 entry points) */
+  FA_KV_F16 = 2    /* K and V are an fp16 cache (IEEE binary16) in p->layout, passed to the plain
+                      entry points; needs p->dtype == FA_BF16. llama.cpp PR #57, commit 2394a4c:
+                      attention reads the cache in place, in the cache's own type (f16 or q8_0).
+                      The library rounds K and V to bf16 (to nearest even) into its workspace
+                      ahead of the kernels, since the tensor cores multiply bf16 by bf16; the
+                      op then computes as on that bf16 K/V, and dK / dV (bf16, or added into the
+                      fp32 accumulators) are the gradients with respect to it. The workspace-size
+                      queries include the copy: 2 x B x Hkv x Sk x D x 2 bytes. */
 } fa_kv_format;
 
 typedef enum fa_layout {
@@ -113,8 +121,8 @@ typedef struct fa_params {
   int32_t deterministic; /* 0 or 1. 1: the backward's dQ is bitwise reproducible from run to run
                             (its per-key-tile partials are added in a fixed order); dK/dV always are.
                             Costs some backward speed and workspace. */
-  int32_t kv_format;  /* fa_kv_format: FA_KV_DTYPE for the plain entry points, FA_KV_Q8_0 for the
-                         _q8 ones (it sizes the workspace) */
+  int32_t kv_format;  /* fa_kv_format: FA_KV_DTYPE or FA_KV_F16 for the plain entry points,
+                         FA_KV_Q8_0 for the _q8 ones (it sizes the workspace) */
   int32_t layout;     /* fa_layout of Q, K, V, O, dO, dQ, dK, dV (and of dk_acc / dv_acc, dk_rows /
                          dv_rows); LSE is always [B, Hq, Sq] and a q8_0 cache's planes always
                          [B, Hkv, Sk, ...] */

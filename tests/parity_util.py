@@ -21,6 +21,9 @@ def torch_dtype(w: wl.Workload):
 def to_device(inputs: dict, w: wl.Workload, device="cuda"):
     dt = torch_dtype(w)
     t = {n: torch.from_numpy(inputs[n]).to(device).to(dt).contiguous() for n in ("q", "k", "v", "do")}
+    if w.kv_format == "f16":   # the fp16 cache as it is (its values are exact in fp16)
+        for n in ("k", "v"):
+            t[n] = torch.from_numpy(inputs[n]).to(device).to(torch.float16).contiguous()
     m = inputs["mask"]
     t["mask"] = None if m is None else torch.from_numpy(m).to(device).contiguous()
     if w.accum:

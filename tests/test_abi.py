@@ -82,7 +82,8 @@ BAD = [
     ("mask_batch", dict(mask_kind=ft.FA_MASK_ADD_F32, mask_batch=3), ft.FA_ERR_INVALID_ARG),
     ("window_negative", dict(window=-1), ft.FA_ERR_INVALID_ARG),
     ("deterministic2", dict(deterministic=2), ft.FA_ERR_INVALID_ARG),
-    ("kv_format", dict(kv_format=2), ft.FA_ERR_INVALID_ARG),
+    ("kv_format", dict(kv_format=3), ft.FA_ERR_INVALID_ARG),
+    ("kv_f16_needs_bf16", dict(kv_format=2, dtype=0), ft.FA_ERR_UNSUPPORTED),
     ("layout", dict(layout=2), ft.FA_ERR_INVALID_ARG),
     ("reserved", dict(reserved=1), ft.FA_ERR_INVALID_ARG),
     ("window_offset_too_big", dict(window=8, q_offset=31), ft.FA_ERR_INVALID_ARG),
@@ -159,3 +160,18 @@ def test_kv_format_must_match_the_entry_point(lib):
     plain = good_params()
     extra = lib.fa_train_fwd_workspace_size(ctypes.byref(p)) - lib.fa_train_fwd_workspace_size(ctypes.byref(plain))
     assert extra >= 2 * 1 * 2 * 130 * 64 * 2
+
+
+def test_f16_cache_workspace_holds_the_bf16_copy(lib):
+    # an fp16 K/V cache under bf16 queries: both passes cast K and V to bf16 in the workspace
+    f16 = good_params(kv_format=ft.FA_KV_F16)
+    plain = good_params()
+    copy = 2 * f16.B * f16.Hkv * f16.Sk * f16.D * 2
+    for size in (lib.fa_train_fwd_workspace_size, lib.fa_train_bwd_workspace_size):
+        extra = size(ctypes.byref(f16)) - size(ctypes.byref(plain))
+        assert copy <= extra < copy + 512
+    # the plain entry points take it; the _q8 ones refuse it
+    kv = ft.FaKvQ8(1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    st = lib.fa_train_fwd_q8(ctypes.byref(f16), 1 << 20, ctypes.byref(kv), None, 1 << 20, 1 << 20, None, 0, None)
+    assert st == ft.FA_ERR_INVALID_ARG and b"_q8" in lib.fa_last_error()
+
