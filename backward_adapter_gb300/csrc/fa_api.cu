@@ -284,6 +284,20 @@ static fa_status kv_spans(const Shape& s, const KvIn& kv, Span* in, int& n) {
   return FA_OK;
 }
 
+// An fp16 cache rounded to bf16 K then V at `dst` (2 x B x Hkv x Sk x D x 2 bytes of workspace), in the
+// call's layout: the tensor cores multiply bf16 by bf16. Points k, v at the copies.
+static fa_status cast_f16_cache(const Shape& s, const KvIn& kv, char* dst, cudaStream_t st, const void*& k,
+                                const void*& v) {
+  const long long n = (long long)s.B * s.Hkv * s.Sk * s.D;
+  char* vdst = dst + (size_t)n * 2;
+  cudaError_t e = launch_f16_to_bf16(kv.k, dst, n, st);
+  if (e == cudaSuccess) e = launch_f16_to_bf16(kv.v, vdst, n, st);
+  if (e != cudaSuccess) return cuda_status(e, "f16 cache cast launch");
+  k = dst;
+  v = vdst;
+  return FA_OK;
+}
+
 static fa_status fwd_common(const fa_params* p, const void* q, const KvIn& kv, const void* mask, void* o, float* lse,
                             void* ws, size_t ws_bytes, void* stream) {
   Shape s;
@@ -309,17 +323,8 @@ static fa_status fwd_common(const fa_params* p, const void* q, const KvIn& kv, c
 
   FwdArgs a{s, q, kv.k, kv.v, mask, o, lse, (cudaStream_t)stream};
   cudaError_t e = cudaSuccess;
-  if (s.kv_format == FA_KV_F16) {
-    // the tensor cores multiply bf16 by bf16: round the cache to a bf16 copy in the call's layout
-    char* kbf = (char*)ws + plan.kvbf_off;
-    char* vbf = kbf + plan.kvbf_bytes / 2;
-    const long long n = (long long)s.B * s.Hkv * s.Sk * s.D;
-    e = launch_f16_to_bf16(kv.k, kbf, n, a.stream);
-    if (e == cudaSuccess) e = launch_f16_to_bf16(kv.v, vbf, n, a.stream);
-    if (e != cudaSuccess) return cuda_status(e, "f16 cache cast launch");
-    a.k = kbf;
-    a.v = vbf;
-  }
+  if (s.kv_format == FA_KV_F16 && (st = cast_f16_cache(s, kv, (char*)ws + plan.kvbf_off, a.stream, a.k, a.v)) != FA_OK)
+    return st;
   if (kv.q8 != nullptr) {
     // every query tile reads every key tile: dequantize the cache once, then run the bf16 kernel on it
     char* kbf = (char*)ws + plan.kvbf_off;
@@ -404,16 +409,8 @@ static fa_status bwd_common(const fa_params* p, const void* q, const KvIn& kv, c
     set_error("a quantized or f16 K/V cache needs the tensor-core path"); return FA_ERR_UNSUPPORTED;
   }
   BwdArgs a{s, q, kv.k, kv.v, mask, o, lse, dO, dq, dk, dv, accum, cs};
-  if (s.kv_format == FA_KV_F16) {
-    char* kbf = (char*)ws + plan.kvbf_off;
-    char* vbf = kbf + plan.kvbf_bytes / 2;
-    const long long n = (long long)s.B * s.Hkv * s.Sk * s.D;
-    cudaError_t e = launch_f16_to_bf16(kv.k, kbf, n, cs);
-    if (e == cudaSuccess) e = launch_f16_to_bf16(kv.v, vbf, n, cs);
-    if (e != cudaSuccess) return cuda_status(e, "f16 cache cast launch");
-    a.k = kbf;
-    a.v = vbf;
-  }
+  if (s.kv_format == FA_KV_F16 && (st = cast_f16_cache(s, kv, (char*)ws + plan.kvbf_off, cs, a.k, a.v)) != FA_OK)
+    return st;
   if (kv.q8 != nullptr) {
     a.kq = kv.q8->k_q;
     a.kd = kv.q8->k_d;
