@@ -120,3 +120,28 @@ def assert_exact_zeros(w: wl.Workload, inputs: dict, got: dict, q_heads=None):
             assert np.all(got["dk"][b][:, cols] == 0) and np.all(got["dv"][b][:, cols] == 0)
         if cols.size and w.accum:
             np.testing.assert_array_equal(got["dk"][b][:, cols], inputs["dk_acc"][b][:, cols])
+
+
+def cache_lse_allowance(w: wl.Workload, inputs: dict, q_heads=None, kv_heads=None) -> float:
+    """Extra LSE tolerance for a q8_0 or fp16 K/V cache: the kernels round each key to bf16, the
+    oracle uses the cache's exact values. LSE is 1-Lipschitz in the scores, so it moves by at most
+    max |scale * <q_i, bf16(k_j) - k_j>| over the compared heads (0 for a bf16 K/V)."""
+    from oracle import set_rows as rows_ref
+    if w.kv_format == "q8_0":
+        k = ref.dequantize_q8_0(*inputs["k_q8"])
+    elif w.kv_format == "f16":
+        k = inputs["k"].astype(np.float64)
+    else:
+        return 0.0
+    dk = rows_ref.to_bf16_bits(k.astype(np.float32)).astype(np.float64) - k
+    G = w.Hq // w.Hkv
+    q = inputs["q"].astype(np.float64)
+    shift = 0.0
+    for h in (range(w.Hq) if q_heads is None else q_heads):
+        kv = h // G
+        if kv_heads is not None and kv not in kv_heads:
+            continue
+        sc = np.einsum("bid,bjd->bij", q[:, h], dk[:, kv]) * w.scale
+        shift = max(shift, float(np.abs(sc).max()))
+    return shift
+

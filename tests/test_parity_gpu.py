@@ -136,9 +136,10 @@ def test_full_dit_workloads_match_oracle(w):
     pu.assert_exact_zeros(w, inputs, got)
 
 
-@pytest.mark.parametrize("w", [wl.CAUSAL_LM, wl.LONG_WINDOW], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [wl.CAUSAL_LM, wl.LONG_WINDOW, wl.LONG_WINDOW_F16], ids=lambda w: w.name)
 def test_full_size_workloads_match_oracle_on_first_and_last_group(w):
-    """At full size the oracle checks the first and last GQA group (every output they own)."""
+    """At full size the oracle checks the first and last GQA group (every output they own); over
+    an fp16 cache LSE may also move by the kernels' bf16 rounding of the keys."""
     inputs = wl.make_inputs(w)
     got = pu.run_gpu(w, pu.to_device(inputs, w))
     G = w.Hq // w.Hkv
@@ -147,4 +148,5 @@ def test_full_size_workloads_match_oracle_on_first_and_last_group(w):
         exp = pu.run_oracle(w, inputs, q_heads=qh, kv_heads=[kv])
         sub = {"o": got["o"][:, qh], "lse": got["lse"][:, qh], "dq": got["dq"][:, qh],
                "dk": got["dk"][:, [kv]], "dv": got["dv"][:, [kv]]}
-        pu.assert_parity(w, sub, exp, where=f" kv-head {kv}")
+        pu.assert_parity(w, sub, exp, where=f" kv-head {kv}",
+                         lse_extra=pu.cache_lse_allowance(w, inputs, q_heads=qh, kv_heads=[kv]))
