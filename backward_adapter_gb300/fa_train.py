@@ -165,6 +165,8 @@ def make_params(q: torch.Tensor, k: torch.Tensor, mask: Optional[torch.Tensor] =
     key positions. window is the sliding-window half-width (0 = none). deterministic makes
     the backward's dQ bitwise reproducible.
     """
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError(f"q and k must be 4-D (got {q.dim()}-D and {k.dim()}-D)")
     if layout == "bhsd":
         B, Hq, Sq, D = q.shape
         Hkv, Sk = k.shape[1], k.shape[2]
@@ -211,19 +213,53 @@ def _need_cuda(*ts):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
 
 
+def _q_shape(p: FaParams, layout: str):
+    return (p.B, p.Hq, p.Sq, p.D) if layout == "bhsd" else (p.B, p.Sq, p.Hq, p.D)
+
+
+def _kv_shape(p: FaParams, layout: str, rows: Optional[int] = None):
+    S = p.Sk if rows is None else rows
+    return (p.B, p.Hkv, S, p.D) if layout == "bhsd" else (p.B, S, p.Hkv, p.D)
+
+
+def _check_tensors(q: torch.Tensor, **expect) -> None:
+    """Every tensor the library will read or write has the shape (and dtype) the parameters imply
+    and lives on q's device: the C ABI receives bare pointers, so a wrong shape would reach the
+    kernels as out-of-bounds accesses. expect maps a name to (tensor or None, shape, dtype or None)."""
+    for name, (t, shape, dtype) in expect.items():
+        if t is None:
+            continue
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+
+
+def _common_expect(p: FaParams, layout: str, q, k=None, v=None, mask=None, o=None, lse=None, do=None, dq=None):
+    qs, ks = _q_shape(p, layout), _kv_shape(p, layout)
+    e = {"k": (k, ks, None), "v": (v, ks, None), "o": (o, qs, q.dtype), "lse": (lse, (p.B, p.Hq, p.Sq), torch.float32),
+         "do": (do, qs, q.dtype), "dq": (dq, qs, q.dtype)}
+    if mask is not None:
+        e["mask"] = (mask, (mask.shape[0], p.Sq, p.Sk), None)
+    return e
+
+
 def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0, deterministic=False, layout="bhsd",
         out=None, lse=None, workspace=None, stream=None):
     """Forward: returns (O [B,Hq,Sq,D] in q's dtype, LSE [B,Hq,Sq] fp32). k and v are in q's dtype,
     or float16 (an fp16 cache) under bfloat16 q."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, k, v, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
                     deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=q.device)
+    _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o=out, lse=lse))
+    _need_cuda(q, k, v, mview, out, lse)
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(out), _ptr(lse),
@@ -236,12 +272,15 @@ def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=No
     """Backward: returns (dQ, dK, dV) in q's dtype (overwriting any given buffers); k and v as in fwd."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
                     deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k, dtype=q.dtype) if dk is None else dk   # q's dtype for an fp16 cache too
     dv = torch.empty_like(v, dtype=q.dtype) if dv is None else dv
+    ks = _kv_shape(p, layout)
+    _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o, lse, do, dq), dk=(dk, ks, q.dtype),
+                   dv=(dv, ks, q.dtype))
+    _need_cuda(q, k, v, o, lse, do, mview, dq, dk, dv)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
@@ -255,12 +294,15 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
     """Accumulating backward: dK/dV are added into fp32 dk_acc/dv_acc in place; returns dQ."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
                     deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
+    ks = _kv_shape(p, layout)
+    _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o, lse, do, dq),
+                   dk_acc=(dk_acc, ks, torch.float32), dv_acc=(dv_acc, ks, torch.float32))
+    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview, dq)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_bwd_accum(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
@@ -280,15 +322,19 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
     """
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview)
     if dk_acc.dtype != torch.float32 or dv_acc.dtype != torch.float32:
         raise TypeError("dk_acc and dv_acc must be float32")
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
                     deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
-    shape = (p.B, p.Hkv, int(n_rows), p.D) if layout == "bhsd" else (p.B, int(n_rows), p.Hkv, p.D)
+    shape = _kv_shape(p, layout, rows=int(n_rows))
     dk_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dk_rows is None else dk_rows
     dv_rows = torch.empty(shape, dtype=q.dtype, device=q.device) if dv_rows is None else dv_rows
+    ks = _kv_shape(p, layout)
+    _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o, lse, do, dq),
+                   dk_acc=(dk_acc, ks, torch.float32), dv_acc=(dv_acc, ks, torch.float32),
+                   dk_rows=(dk_rows, shape, q.dtype), dv_rows=(dv_rows, shape, q.dtype))
+    _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview, dq, dk_rows, dv_rows)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_bwd_accum_rows(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
@@ -298,7 +344,6 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
 
 
 def _kv_q8(k_q, k_d, v_q, v_d) -> FaKvQ8:
-    _need_cuda(k_q, k_d, v_q, v_d)
     if k_q.dtype != torch.int8 or v_q.dtype != torch.int8:
         raise TypeError("k_q and v_q must be int8 [B, Hkv, Sk, D]")
     if k_d.dtype != torch.float16 or v_d.dtype != torch.float16:
@@ -311,17 +356,24 @@ def _cache_shape_view(k_q, layout):
     return k_q if layout == "bhsd" else k_q.transpose(1, 2)
 
 
+def _q8_expect(p: FaParams, k_q, k_d, v_q, v_d):
+    planes, scales = (p.B, p.Hkv, p.Sk, p.D), (p.B, p.Hkv, p.Sk, p.D // 32)
+    return {"k_q": (k_q, planes, torch.int8), "v_q": (v_q, planes, torch.int8),
+            "k_d": (k_d, scales, torch.float16), "v_d": (v_d, scales, torch.float16)}
+
+
 def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offset=None, window=0, layout="bhsd",
            out=None, lse=None, workspace=None, stream=None):
     """Forward over a q8_0 K/V cache (int8 values k_q/v_q, fp16 scales k_d/v_d per 32 features)."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, mview)
     kv = _kv_q8(k_q, k_d, v_q, v_d)
     p = make_params(q, _cache_shape_view(k_q, layout), mask, scale=scale, causal=causal, q_offset=q_offset,
                     window=window, kv_format=FA_KV_Q8_0, layout=layout)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors(q, **_common_expect(p, layout, q, mask=mask, o=out, lse=lse), **_q8_expect(p, k_q, k_d, v_q, v_d))
+    _need_cuda(q, mview, out, lse, k_q, k_d, v_q, v_d)
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     _check(lib.fa_train_fwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(out), _ptr(lse),
@@ -336,11 +388,17 @@ def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=F
     K/V are added into them (returns dQ); otherwise returns (dQ, dK, dV) in q's dtype."""
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, o, lse, do, mview, dk_acc, dv_acc)
     kv = _kv_q8(k_q, k_d, v_q, v_d)
     p = make_params(q, _cache_shape_view(k_q, layout), mask, scale=scale, causal=causal, q_offset=q_offset,
                     window=window, deterministic=deterministic, kv_format=FA_KV_Q8_0, layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
+    if (dk_acc is None) != (dv_acc is None):
+        raise ValueError("give both dk_acc and dv_acc, or neither")
+    ks = _kv_shape(p, layout)
+    _check_tensors(q, **_common_expect(p, layout, q, mask=mask, o=o, lse=lse, do=do, dq=dq),
+                   **_q8_expect(p, k_q, k_d, v_q, v_d), dk_acc=(dk_acc, ks, torch.float32),
+                   dv_acc=(dv_acc, ks, torch.float32), dk=(dk, ks, q.dtype), dv=(dv, ks, q.dtype))
+    _need_cuda(q, o, lse, do, mview, dq, dk_acc, dv_acc, dk, dv, k_q, k_d, v_q, v_d)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     if dk_acc is not None:
@@ -358,7 +416,6 @@ def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=F
 
 def set_rows_backward(acc: torch.Tensor, idx: torch.Tensor, out_dtype=torch.bfloat16, out=None, stream=None):
     """SET_ROWS backward: out[b, h, r] = acc[b, h, idx[r]] (acc fp32 [B, H, S, D], idx int64 [n])."""
-    _need_cuda(acc, idx)
     if acc.dtype != torch.float32 or acc.dim() != 4:
         raise TypeError("acc must be float32 [B, H, S, D]")
     if idx.dtype != torch.int64 or idx.dim() != 1:
@@ -366,7 +423,9 @@ def set_rows_backward(acc: torch.Tensor, idx: torch.Tensor, out_dtype=torch.bflo
     B, H, S, D = acc.shape
     if out is None:
         out = torch.empty((B, H, idx.shape[0], D), dtype=out_dtype, device=acc.device)
-    _need_cuda(out)
+    if tuple(out.shape) != (B, H, idx.shape[0], D):
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected {(B, H, idx.shape[0], D)}")
+    _need_cuda(acc, idx, out)
     _check(load_library().fa_set_rows_backward(_ptr(acc), B, H, S, D, _ptr(idx), idx.shape[0], _ptr(out),
                                                _dtype_code(out), _stream(acc.device, stream)))
     return out
@@ -414,12 +473,15 @@ def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_o
     """
     lib = load_library()
     mview, _, _ = _mask_view(mask)
-    _need_cuda(q, k, v, o, lse, do, mview)
     p = make_params(q, k, mask, scale=scale, causal=causal, q_offset=q_offset, window=window,
                     deterministic=deterministic, kv_format=_kv_format(q, k, v), layout=layout)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k, dtype=q.dtype) if dk is None else dk   # q's dtype for an fp16 cache too
     dv = torch.empty_like(v, dtype=q.dtype) if dv is None else dv
+    ks = _kv_shape(p, layout)
+    _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o, lse, do, dq), dk=(dk, ks, q.dtype),
+                   dv=(dv, ks, q.dtype))
+    _need_cuda(q, k, v, o, lse, do, mview, dq, dk, dv)
     _check(lib.fa_train_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
                                     _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(q.device, stream)))
     return dq, dk, dv
