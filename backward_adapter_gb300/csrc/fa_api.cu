@@ -28,6 +28,11 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 constexpr int kMaxSeq = 1 << 24;
+// Largest element count of one tensor (2^40: terabytes, more than a GB300 holds). Keeps every byte
+// count of the validation and every 64-bit offset in the kernels far from overflow.
+constexpr double kMaxElems = 1099511627776.0;
+
+bool too_large(double a, double b, double c, double d) { return a * b * c * d > kMaxElems; }
 
 fa_status check_params(const fa_params* p, Shape& s) {
   g_last_error[0] = '\0';
@@ -64,6 +69,10 @@ fa_status check_params(const fa_params* p, Shape& s) {
     set_error("layout=%d invalid", p->layout); return FA_ERR_INVALID_ARG;
   }
   if (p->reserved != 0) { set_error("reserved field must be 0"); return FA_ERR_INVALID_ARG; }
+  if (too_large(p->B, p->Hq, p->Sq, p->D) || too_large(p->B, p->Hkv, p->Sk, p->D) ||
+      (p->mask_kind != FA_MASK_NONE && too_large(p->mask_batch, p->Sq, p->Sk, 1))) {
+    set_error("a tensor of these shapes would hold more than 2^40 elements"); return FA_ERR_INVALID_ARG;
+  }
   const bool positioned = p->causal || p->window > 0;
   if (positioned && (p->q_offset < 0 || p->q_offset + p->Sq > p->Sk)) {
     set_error("q_offset=%lld with Sq=%d needs 0 <= q_offset and q_offset + Sq <= Sk=%d",
@@ -476,6 +485,9 @@ fa_status fa_set_rows_backward(const float* acc, int32_t B, int32_t H, int32_t S
   if (D < 4 || D > 1024 || D % 4 != 0) { set_error("D=%d: a multiple of 4 in [4, 1024]", D); return FA_ERR_INVALID_ARG; }
   if (n_rows < 0) { set_error("n_rows=%d must be >= 0", n_rows); return FA_ERR_INVALID_ARG; }
   if (out_dtype != FA_F32 && out_dtype != FA_BF16) { set_error("out_dtype=%d invalid", out_dtype); return FA_ERR_INVALID_ARG; }
+  if (too_large(B, H, S, D) || too_large(B, H, n_rows, D)) {
+    set_error("acc or out would hold more than 2^40 elements"); return FA_ERR_INVALID_ARG;
+  }
   if (n_rows == 0) return FA_OK;
   if (acc == nullptr || idx == nullptr || out == nullptr) { set_error("acc, idx and out must be non-NULL"); return FA_ERR_INVALID_ARG; }
   if ((uintptr_t)acc % 16 != 0 || (uintptr_t)out % 16 != 0 || (uintptr_t)idx % 8 != 0) {

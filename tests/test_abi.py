@@ -86,6 +86,10 @@ BAD = [
     ("kv_f16_needs_bf16", dict(kv_format=2, dtype=0), ft.FA_ERR_UNSUPPORTED),
     ("layout", dict(layout=2), ft.FA_ERR_INVALID_ARG),
     ("reserved", dict(reserved=1), ft.FA_ERR_INVALID_ARG),
+    ("q_too_large", dict(B=65535, Hq=65535, Hkv=65535, Sq=1 << 16), ft.FA_ERR_INVALID_ARG),
+    ("kv_too_large", dict(B=1024, Hq=4096, Hkv=4096, Sk=1 << 24), ft.FA_ERR_INVALID_ARG),
+    ("mask_too_large", dict(B=65535, Sq=1 << 20, Sk=1 << 20, mask_kind=ft.FA_MASK_BOOL_U8, mask_batch=65535),
+     ft.FA_ERR_INVALID_ARG),
     ("window_offset_too_big", dict(window=8, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_too_big", dict(causal=1, q_offset=31), ft.FA_ERR_INVALID_ARG),
     ("causal_offset_negative", dict(causal=1, q_offset=-1), ft.FA_ERR_INVALID_ARG),
@@ -174,4 +178,9 @@ def test_f16_cache_workspace_holds_the_bf16_copy(lib):
     kv = ft.FaKvQ8(1 << 20, 1 << 20, 1 << 20, 1 << 20)
     st = lib.fa_train_fwd_q8(ctypes.byref(f16), 1 << 20, ctypes.byref(kv), None, 1 << 20, 1 << 20, None, 0, None)
     assert st == ft.FA_ERR_INVALID_ARG and b"_q8" in lib.fa_last_error()
+
+
+def test_set_rows_backward_refuses_sizes_that_overflow(lib):
+    st = lib.fa_set_rows_backward(1 << 20, 65535, 32767, 1 << 24, 1024, 1 << 20, 1, 2 << 20, ft.FA_BF16, None)
+    assert st == ft.FA_ERR_INVALID_ARG and b"2^40" in lib.fa_last_error()
 
