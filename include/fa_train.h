@@ -47,6 +47,9 @@
  *     flight at once must not share a workspace.
  *   - Outputs must not alias inputs or each other.
  *
+ * Limits: B and Hq at most 65535, Sq and Sk at most 2^24, D 64 or 128, and no tensor of the call
+ * (Q, K, V, the mask, the gradients) above 2^40 elements.
+ *
  * Errors: parameters are validated before anything is enqueued. A rejected call
  * returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE and leaves
  * every buffer untouched. A failed launch returns FA_ERR_CUDA. fa_last_error()
