@@ -5,7 +5,9 @@
 //
 // One CTA takes 256 query rows (two 128-row tiles Q0, Q1) of one (batch, query
 // head) and walks the visible 128-key tiles of its key/value head:
-//   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of slots;
+//   warp 0      TMA producer: Q0/Q1 once, then a ring of stages, each holding V of
+//               one key tile and K of the next (one wait per tile for the issuer; the
+//               stage is released by the completion of the tile's last MMA group);
 //   warp 1      MMA issuer (one thread) and TMEM owner:
 //                 S_t = Q_t K_j^T  (SMEM x SMEM -> TMEM fp32)
 //                 O_t += P_t V_j   (P from TMEM, V from SMEM -> TMEM fp32);
@@ -66,6 +68,7 @@ struct FwdSmem {
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16 (one 128B-swizzled box)
   static constexpr int kTileBytes = kBM * D * 2;         // one Q or K or V tile
   static constexpr int kSlots = D == 128 ? 4 : 8;        // ring slots for K and V tiles
+  static constexpr int kStages = kSlots / 2;             // a stage: V of one key tile and K of the next
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
@@ -115,9 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   uint8_t* sKV = smem + L::kKVOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* bar_q = bars + 0;
-  uint64_t* bar_full = bars + 1;                  // [kSlots]
-  uint64_t* bar_empty = bar_full + L::kSlots;     // [kSlots]
-  uint64_t* bar_s = bar_empty + L::kSlots;        // [2]
+  uint64_t* bar_full = bars + 1;                  // [kStages]
+  uint64_t* bar_s = bar_full + L::kStages;        // [2]
   uint64_t* bar_p = bar_s + 2;                    // [2]
   uint64_t* bar_o = bar_p + 2;                    // [2]
   uint64_t* bar_done = bar_o + 2;                 // [1]
@@ -142,9 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int i = 0; i < L::kSlots; ++i) {
+    for (int i = 0; i < L::kStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
@@ -175,28 +176,41 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       for (int t = 0; t < 2; ++t)
         for (int box = 0; box < D / 64; ++box)
           tma_load_4d(sQ + t * L::kTileBytes + box * L::kBoxBytes, &p.tm_q, bar_q, box * 64, q_row0 + t * kBM, h, b);
-      int slot = 0;
-      uint32_t phase = 0;
-      uint32_t used_mask = 0, phase_mask = 0;  // per slot: filled at least once / parity of its last fill
-      for (int j = kr.begin; j < kr.end; ++j) {
-        if (skip_tile(p, mb, qt0, j)) continue;
-        bool ok = true;
-        for (int which = 0; which < 2 && ok; ++which) {
-          if (!mbar_wait(&bar_empty[slot], phase ^ 1, abort_flag, p.status, 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bar_full[slot], L::kTileBytes);
-          const CUtensorMap* map = which == 0 ? &p.tm_k : &p.tm_v;
-          for (int box = 0; box < D / 64; ++box)
-            tma_load_4d(sKV + slot * L::kTileBytes + box * L::kBoxBytes, map, &bar_full[slot], box * 64, j * kBN,
+      // Stage st of the ring holds V of the (st-1)-th visible key tile and K of the st-th: the
+      // MMAs of one step read exactly one stage, so a step costs the issuer one wait. The stage is
+      // free again once S_1 of its step has completed (the step's PV and S MMAs, issued before it,
+      // have then read V and K): the producer waits for those completions of bar_s[1] one by one,
+      // in order, so the barrier's phase parity cannot alias.
+      uint32_t used_mask = 0, phase_mask = 0;  // per stage: filled at least once / parity of its last fill
+      int st = 0, prev = -1, released = 0;
+      for (int j = kr.begin;; ++j) {
+        while (j < kr.end && skip_tile(p, mb, qt0, j)) ++j;
+        const bool has_k = j < kr.end;
+        if (!has_k && prev < 0) break;
+        const int sb = st % L::kStages;
+        const uint32_t ph = (st / L::kStages) & 1;
+        bool free_ok = true;
+        for (; free_ok && released <= st - L::kStages; ++released)
+          free_ok = mbar_wait(&bar_s[1], released & 1, abort_flag, p.status, 1);
+        if (!free_ok) break;
+        mbar_arrive_expect_tx(&bar_full[sb], (prev >= 0 ? L::kTileBytes : 0) + (has_k ? L::kTileBytes : 0));
+        for (int box = 0; box < D / 64; ++box) {
+          if (prev >= 0)
+            tma_load_4d(sKV + (2 * sb + 1) * L::kTileBytes + box * L::kBoxBytes, &p.tm_v, &bar_full[sb], box * 64,
+                        prev * kBN, kvh, b);
+          if (has_k)
+            tma_load_4d(sKV + 2 * sb * L::kTileBytes + box * L::kBoxBytes, &p.tm_k, &bar_full[sb], box * 64, j * kBN,
                         kvh, b);
-          used_mask |= 1u << slot;
-          phase_mask = (phase_mask & ~(1u << slot)) | (phase << slot);
-          if (++slot == L::kSlots) { slot = 0; phase ^= 1; }
         }
-        if (!ok) break;
+        used_mask |= 1u << sb;
+        phase_mask = (phase_mask & ~(1u << sb)) | (ph << sb);
+        ++st;
+        if (!has_k) break;
+        prev = j;
       }
       // Drain: every copy this thread issued has landed before the block can exit.
       mbar_wait(bar_q, 0, nullptr, p.status, 2);
-      for (int i = 0; i < L::kSlots; ++i)
+      for (int i = 0; i < L::kStages; ++i)
         if (used_mask >> i & 1u) mbar_wait(&bar_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 3);
     }
   } else if (warp == 1) {
@@ -225,41 +239,34 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.status, 10);
       tc_fence_after();
-      int idx = 0, c = 0;  // tiles processed, slots consumed
-      int v_slot = 0;
-      uint32_t v_phase = 0;
+      int idx = 0;  // visible key tiles processed = ring stages consumed
       for (int j = kr.begin; ok && j < kr.end; ++j) {
         if (skip_tile(p, mb, qt0, j)) continue;
-        const int k_slot = c % L::kSlots;
-        const uint32_t k_phase = (c / L::kSlots) & 1;
-        if (!(ok = mbar_wait(&bar_full[k_slot], k_phase, abort_flag, p.status, 11))) break;
+        const int sb = idx % L::kStages;
+        if (!(ok = mbar_wait(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 11))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
           if (idx > 0) {
             if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 12))) break;
-            if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 13))) break;
             tc_fence_after();
-            issue_pv(t, v_slot, idx - 1 > 0);
+            issue_pv(t, 2 * sb + 1, idx - 1 > 0);
           }
-          issue_s(t, k_slot);
+          issue_s(t, 2 * sb);
           mma_commit(&bar_s[t]);
         }
         if (!ok) break;
-        if (idx > 0) mma_commit(&bar_empty[v_slot]);
-        mma_commit(&bar_empty[k_slot]);
-        v_slot = (c + 1) % L::kSlots;
-        v_phase = ((c + 1) / L::kSlots) & 1;
-        c += 2;
         ++idx;
       }
       if (ok && idx > 0) {
+        // the last stage holds only V of the last visible tile
+        const int sb = idx % L::kStages;
+        ok = mbar_wait(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 15);
 #pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
           if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 14))) break;
-          if (t == 0 && !(ok = mbar_wait(&bar_full[v_slot], v_phase, abort_flag, p.status, 15))) break;
           tc_fence_after();
-          issue_pv(t, v_slot, idx - 1 > 0);
+          issue_pv(t, 2 * sb + 1, idx - 1 > 0);
           mma_commit(&bar_o[t]);
         }
       }
