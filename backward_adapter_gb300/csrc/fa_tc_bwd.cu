@@ -80,7 +80,8 @@ struct BwdCfg {
   static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
   static constexpr int DQ_CHUNKS = (DQ_TRANSPOSED ? BQ : D) / 32;   // 32-column TMEM chunks of the dQ partial
   static constexpr int NSTAGE = 2;                      // Q/dO ring depth
-  static constexpr int NDS = 1;                         // dS^T shared-memory buffers
+  static constexpr int NDS = 1;                         // dS^T shared-memory buffers (the dQ MMA of a
+                                                        // step completes before the next dS^T is written)
   // shared memory (bytes)
   static constexpr int KV_BOX = 128 * 128;              // 128 rows x 128 B
   static constexpr int KV_TILE = kBN * D * 2;
@@ -196,8 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_p_half = bar_p_full + C::NBUF;          // 1: P^T / dS^T of the step's first 64 queries
   uint64_t* bar_dq_full = bar_p_half + 1;               // NBUF
   uint64_t* bar_dq_free = bar_dq_full + C::NBUF;        // NBUF
-  uint64_t* bar_ds_free = bar_dq_free + C::NBUF;        // NDS: the dQ MMA has read that dS^T buffer
-  uint64_t* bar_mma_done = bar_ds_free + C::NDS;        // 1
+  uint64_t* bar_mma_done = bar_dq_free + C::NBUF;       // 1
   uint64_t* bar_stage_full = bar_mma_done + 1;          // 1: the 4 stager warps filled the dQ staging
   uint64_t* bar_s_full = bar_stage_full + 1;            // NBUF: S^T of the block is in TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s_full + C::NBUF);
@@ -250,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       mbar_init(&bar_dq_full[i], 1);
       mbar_init(&bar_dq_free[i], 4);
     }
-    for (int i = 0; i < C::NDS; ++i) mbar_init(&bar_ds_free[i], 1);
     mbar_init(bar_p_half, 8);
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_stage_full, 4);
@@ -290,14 +289,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           tma_load_4d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvh, b);
         }
       }
+      // D = 128: the slot of step st is free once dK of step st - NSTAGE has read it, which the
+      // completion of that step's dQ MMA (issued after dK) implies; those completions of bar_dq_full
+      // are waited for one by one, in order, so its phase parity cannot alias. D = 64: the stager
+      // hands the slot back once the dQ partial staged in it has been reduced.
       uint32_t used_mask = 0, phase_mask = 0;
+      int released = 0;
       StepIter it;
       it.init(G, iend, BQ, ibeg, s.deterministic != 0);
       for (int st = 0; it.valid(); it.next()) {
         if (step_skipped(it)) continue;
         const int slot = st % C::NSTAGE;
         const uint32_t ph = (st / C::NSTAGE) & 1;
-        if (!mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101)) break;
+        bool free_ok = true;
+        if (C::RED_DQ) {
+          for (; free_ok && released <= st - C::NSTAGE; ++released)
+            free_ok = mbar_wait(&bar_dq_full[0], released & 1, abort_flag, p.status, 101);
+        } else {
+          free_ok = mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101);
+        }
+        if (!free_ok) break;
         mbar_arrive_expect_tx(&bar_qdo_full[slot], 2 * C::Q_TILE);
         uint8_t* sq = smem + C::OFF_STAGE + slot * 2 * C::Q_TILE;
         const int qh = kvh * G + it.hh;   // query head
@@ -389,8 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           else
             mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
         }
-        mma_commit(&bar_dq_full[st % C::NBUF]);
-        mma_commit(&bar_ds_free[st % C::NDS]);
+        mma_commit(&bar_dq_full[st % C::NBUF]);   // also frees the dS^T tile and, D = 128, the Q/dO slot
       };
 
       // Issue whichever MMA group is ready; none that waits holds back one that is ready. With one
@@ -412,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           progressed = true;
         } else if (na > ns && mbar_test(&bar_p_full[0], ns & 1)) {
           issue_dvdk(ns, 1);
-          if (C::RED_DQ) mma_commit(&bar_qdo_empty[ns % C::NSTAGE]);   // dV / dK were the slot's last readers
           issue_dq(ns++);
           progressed = true;
         } else if (np < nt && (np == 0 || mbar_test(&bar_dq_free[0], (np - 1) & 1))) {
@@ -498,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       const int buf = st % C::NBUF, slot = st % C::NSTAGE, dsb = st % C::NDS;
       ok = mbar_wait(&bar_s_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 130);
       ok = ok && mbar_wait(&bar_lsed_full[slot], (st / C::NSTAGE) & 1, abort_flag, p.status, 131);
-      if (st >= C::NDS) ok = ok && mbar_wait(&bar_ds_free[dsb], ((st - C::NDS) / C::NDS) & 1, abort_flag, p.status, 132);
+      // the dQ MMA of the previous step has read the dS^T tile (its completion on bar_dq_full)
+      if (st > 0) ok = ok && mbar_wait(&bar_dq_full[0], (st - 1) & 1, abort_flag, p.status, 132);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
