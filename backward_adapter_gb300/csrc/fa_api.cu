@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "fa_train.h"
 #include "fa_internal.h"
@@ -169,6 +170,9 @@ void set_error_message(const char* msg) { set_error("%s", msg); }
 unsigned* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  // host threads making their first call at the same time fill the per-device cache under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
   if (g_status_ptr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fa_device_status) != cudaSuccess) return nullptr;

@@ -193,6 +193,12 @@ def bwd_workspace_size(p: FaParams) -> int:
     return int(load_library().fa_train_bwd_workspace_size(ctypes.byref(p)))
 
 
+def _on_device(t: torch.Tensor):
+    """The library launches on, and keeps its per-device state for, the current CUDA device:
+    make it the device the call's tensors live on."""
+    return torch.cuda.device(t.device)
+
+
 def _stream(device: torch.device, stream) -> int:
     if stream is None:
         return torch.cuda.current_stream(device).cuda_stream
@@ -262,8 +268,9 @@ def fwd(q, k, v, mask=None, *, scale=None, causal=False, q_offset=None, window=0
     _need_cuda(q, k, v, mview, out, lse)
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
-    _check(lib.fa_train_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(out), _ptr(lse),
-                            _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(out), _ptr(lse),
+                                _ptr(ws), ws_bytes, _stream(q.device, stream)))
     return out, lse
 
 
@@ -283,9 +290,10 @@ def bwd(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_offset=No
     _need_cuda(q, k, v, o, lse, do, mview, dq, dk, dv)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
-    _check(lib.fa_train_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
-                            _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes,
-                            _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes,
+                                _stream(q.device, stream)))
     return dq, dk, dv
 
 
@@ -305,9 +313,10 @@ def bwd_accum(q, k, v, o, lse, do, dk_acc, dv_acc, mask=None, *, scale=None, cau
     _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview, dq)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
-    _check(lib.fa_train_bwd_accum(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
-                                  _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
-                                  _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_bwd_accum(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                      _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
+                                      _stream(q.device, stream)))
     return dq
 
 
@@ -337,9 +346,10 @@ def bwd_accum_rows(q, k, v, o, lse, do, dk_acc, dv_acc, rows_begin: int, n_rows:
     _need_cuda(q, k, v, o, lse, do, dk_acc, dv_acc, mview, dq, dk_rows, dv_rows)
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
-    _check(lib.fa_train_bwd_accum_rows(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
-                                       _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), int(rows_begin), int(n_rows),
-                                       _ptr(dk_rows), _ptr(dv_rows), _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_bwd_accum_rows(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
+                                           _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), int(rows_begin), int(n_rows),
+                                           _ptr(dk_rows), _ptr(dv_rows), _ptr(ws), ws_bytes, _stream(q.device, stream)))
     return dq, dk_rows, dv_rows
 
 
@@ -376,8 +386,9 @@ def fwd_q8(q, k_q, k_d, v_q, v_d, mask=None, *, scale=None, causal=False, q_offs
     _need_cuda(q, mview, out, lse, k_q, k_d, v_q, v_d)
     ws_bytes = fwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
-    _check(lib.fa_train_fwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(out), _ptr(lse),
-                               _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_fwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(out), _ptr(lse),
+                                   _ptr(ws), ws_bytes, _stream(q.device, stream)))
     return out, lse
 
 
@@ -402,15 +413,17 @@ def bwd_q8(q, k_q, k_d, v_q, v_d, o, lse, do, mask=None, *, scale=None, causal=F
     ws_bytes = bwd_workspace_size(p)
     ws = _workspace(ws_bytes, q.device, workspace)
     if dk_acc is not None:
-        _check(lib.fa_train_bwd_accum_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
-                                         _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
-                                         _stream(q.device, stream)))
+        with _on_device(q):
+            _check(lib.fa_train_bwd_accum_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
+                                             _ptr(do), _ptr(dq), _ptr(dk_acc), _ptr(dv_acc), _ptr(ws), ws_bytes,
+                                             _stream(q.device, stream)))
         return dq
     shape = tuple(_cache_shape_view(k_q, layout).shape)   # dK / dV in the call's layout
     dk = torch.empty(shape, dtype=q.dtype, device=q.device) if dk is None else dk
     dv = torch.empty(shape, dtype=q.dtype, device=q.device) if dv is None else dv
-    _check(lib.fa_train_bwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
-                               _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes, _stream(q.device, stream)))
+    with _on_device(q):
+        _check(lib.fa_train_bwd_q8(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(mview), _ptr(o), _ptr(lse),
+                                   _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes, _stream(q.device, stream)))
     return dq, dk, dv
 
 
@@ -426,8 +439,9 @@ def set_rows_backward(acc: torch.Tensor, idx: torch.Tensor, out_dtype=torch.bflo
     if tuple(out.shape) != (B, H, idx.shape[0], D):
         raise ValueError(f"out has shape {tuple(out.shape)}, expected {(B, H, idx.shape[0], D)}")
     _need_cuda(acc, idx, out)
-    _check(load_library().fa_set_rows_backward(_ptr(acc), B, H, S, D, _ptr(idx), idx.shape[0], _ptr(out),
-                                               _dtype_code(out), _stream(acc.device, stream)))
+    with _on_device(acc):
+        _check(load_library().fa_set_rows_backward(_ptr(acc), B, H, S, D, _ptr(idx), idx.shape[0], _ptr(out),
+                                                   _dtype_code(out), _stream(acc.device, stream)))
     return out
 
 
@@ -482,6 +496,8 @@ def bwd_noalloc(q, k, v, o, lse, do, mask=None, *, scale=None, causal=False, q_o
     _check_tensors(q, **_common_expect(p, layout, q, k, v, mask, o, lse, do, dq), dk=(dk, ks, q.dtype),
                    dv=(dv, ks, q.dtype))
     _need_cuda(q, k, v, o, lse, do, mview, dq, dk, dv)
-    _check(lib.fa_train_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o), _ptr(lse),
-                                    _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(q.device, stream)))
+    # the library finds its static scratch, and launches, on the current device: make it q's
+    with _on_device(q):
+        _check(lib.fa_train_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(mview), _ptr(o),
+                                        _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(q.device, stream)))
     return dq, dk, dv

@@ -44,6 +44,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload-steps", type=int, default=30,
+                    help="timed steps of each of the other workloads in by_workload")
+    ap.add_argument("--no-by-workload", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise reproducible dQ (partials added in a fixed key-tile order)")
     return ap.parse_args(argv)
@@ -255,6 +258,156 @@ def gbs(nbytes, ms):
     return nbytes / (ms * 1e-3) / 1e9 if ms > 0 else None
 
 
+KERNELS = ("fwd", "bwd_main", "bwd_dsum", "bwd_dq_convert", "mask_classify")
+
+
+def stats(ms):
+    """mean, median and min of a list of times (ms); None when there are none."""
+    if not ms:
+        return None
+    return {"mean": statistics.mean(ms), "median": statistics.median(ms), "min": min(ms)}
+
+
+class Prepared:
+    """Device inputs, outputs and the two public-API calls of one step of a workload."""
+
+    def __init__(self, ft, torch, w, dev, deterministic=False):
+        self.w = w
+        inputs = wl.make_inputs(w)
+        self.inputs = inputs
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.es = 2 if w.dtype == "bf16" else 4
+        self.q8 = q8 = w.kv_format == "q8_0"
+        host = {n: torch.from_numpy(inputs[n]).to(dt).pin_memory()
+                for n in (("q", "do") if q8 else ("q", "k", "v", "do"))}
+        if w.kv_format == "f16":   # an fp16 K/V cache, read in place (the library casts it for the tensor cores)
+            for n in ("k", "v"):
+                host[n] = torch.from_numpy(inputs[n]).to(torch.float16).pin_memory()
+        if q8:   # the K/V cache in its own format: int8 values and fp16 scales, read in place
+            for n in ("k", "v"):
+                qv, dv_ = inputs[n + "_q8"]
+                host[n + "_q"] = torch.from_numpy(qv).pin_memory()
+                host[n + "_d"] = torch.from_numpy(dv_).pin_memory()
+        if inputs["mask"] is not None:
+            host["mask"] = torch.from_numpy(inputs["mask"]).pin_memory()
+        self.host = host
+        self.d = d = {n: t.to(dev) for n, t in host.items()}
+        self.kw = kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window,
+                            deterministic=deterministic)
+        kv_format = {"q8_0": ft.FA_KV_Q8_0, "f16": ft.FA_KV_F16}.get(w.kv_format, ft.FA_KV_DTYPE)
+        p = ft.make_params(d["q"], d["k_q" if q8 else "k"], d.get("mask"), kv_format=kv_format, **kw)
+        self.ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
+        self.o = torch.empty_like(d["q"])
+        self.lse = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(d["q"])
+        self.dk_rows = self.dv_rows = None
+        if w.accum:
+            self.dk = torch.from_numpy(inputs["dk_acc"]).to(dev)
+            self.dv = torch.from_numpy(inputs["dv_acc"]).to(dev)
+            # the chunk's own K/V rows (the last Sq keys of the window) are read back from the
+            # accumulator in the same kernel (fused SET_ROWS backward)
+            rows_shape = (w.B, w.Hkv, w.Sq, w.D)
+            self.dk_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
+            self.dv_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
+        else:
+            kv_shape = (w.B, w.Hkv, w.Sk, w.D)
+            self.dk = torch.empty(kv_shape, dtype=dt, device=dev)
+            self.dv = torch.empty(kv_shape, dtype=dt, device=dev)
+        self.ft = ft
+
+    def fwd_call(self, src, o_, lse_):
+        ft, w = self.ft, self.w
+        fkw = {k_: v_ for k_, v_ in self.kw.items() if k_ != "deterministic"}
+        if self.q8:
+            return ft.fwd_q8(src["q"], src["k_q"], src["k_d"], src["v_q"], src["v_d"], src.get("mask"), out=o_,
+                             lse=lse_, workspace=self.ws_f, **fkw)
+        return ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=o_, lse=lse_, workspace=self.ws_f,
+                      **self.kw)
+
+    def bwd_call(self, src, o_, lse_, dq_, dk_, dv_):
+        ft, w, kw = self.ft, self.w, self.kw
+        if self.q8:
+            kv = (src["k_q"], src["k_d"], src["v_q"], src["v_d"])
+            if w.accum:
+                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk_acc=dk_, dv_acc=dv_,
+                          workspace=self.ws_b, **kw)
+            else:
+                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
+                          workspace=self.ws_b, **kw)
+        elif w.accum:
+            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, w.q_offset, w.Sq,
+                              src.get("mask"), dq=dq_, dk_rows=self.dk_rows, dv_rows=self.dv_rows,
+                              workspace=self.ws_b, **kw)
+        else:
+            ft.bwd(src["q"], src["k"], src["v"], o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
+                   workspace=self.ws_b, **kw)
+
+    def step(self):
+        self.fwd_call(self.d, self.o, self.lse)
+        self.bwd_call(self.d, self.o, self.lse, self.dq, self.dk, self.dv)
+
+
+def timed_steps(torch, ft, prep, K, W, flush):
+    """W untimed steps, then K timed ones with the L2 flushed before each (outside the events).
+    Returns (per-step ms list, {kernel: per-step ms list}, library launches in the K steps)."""
+    for _ in range(W):
+        prep.step()
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [(ev(), ev()) for _ in range(K)]
+    kids = {"fwd": ft.FA_KERNEL_FWD, "bwd_main": ft.FA_KERNEL_BWD_MAIN, "bwd_dsum": ft.FA_KERNEL_BWD_DSUM,
+            "bwd_dq_convert": ft.FA_KERNEL_BWD_DQ_CONVERT, "mask_classify": ft.FA_KERNEL_MASK_CLASSIFY}
+    kern = {name: [(ev(), ev()) for _ in range(K)] for name in kids}
+    # torch creates the CUDA event lazily at its first record(): materialise every handle
+    # before the library is asked to record it
+    for evs in kern.values():
+        for a_, b_ in evs:
+            a_.record()
+            b_.record()
+    torch.cuda.synchronize()
+    launches0 = ft.profile_launch_count()
+    for i in range(K):
+        flush.zero_()                      # evict L2 between timed steps (not inside the step events)
+        for name, evs in kern.items():
+            ft.profile_set_events(kids[name], *evs[i])
+        step_ev[i][0].record()
+        prep.step()
+        step_ev[i][1].record()
+    torch.cuda.synchronize()
+    launches = ft.profile_launch_count() - launches0
+    for kid in kids.values():
+        ft.profile_set_events(kid, None, None)
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    kern_ms = {}
+    for name, evs in kern.items():
+        # a pair the library recorded during step i starts inside that step; a pair it never
+        # recorded still holds its materialising record from before the timed steps (this path
+        # does not launch that kernel)
+        kern_ms[name] = [a.elapsed_time(b) for (a, b), (s0, _) in zip(evs, step_ev) if s0.elapsed_time(a) >= 0.0]
+    return step_ms, kern_ms, launches
+
+
+def workload_summary(w, fl, step_ms, kern_ms, peak):
+    """One workload's line: step, forward and backward times (mean / median / min), TFLOP/s on the
+    median and its fraction of the dense bf16 peak."""
+    st = stats(step_ms)
+    ks = {n: stats(v) for n, v in kern_ms.items() if v}
+    bwd = [sum(x) for x in zip(*(kern_ms[n] for n in ("bwd_main", "bwd_dsum", "bwd_dq_convert") if kern_ms[n]))]
+    out = {"config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "dtype": w.dtype,
+                      "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask,
+                      "accum": w.accum, "kv_format": w.kv_format},
+           "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
+           "step_ms": st, "kernel_ms": ks,
+           "tflops": fl["total"] / (st["median"] * 1e-3) / 1e12,
+           "frac_of_peak": fl["total"] / (st["median"] * 1e-3) / 1e12 / peak}
+    if ks.get("fwd"):
+        out["fwd_tflops"] = fl["fwd"] / (ks["fwd"]["median"] * 1e-3) / 1e12
+    if bwd:
+        out["bwd_tflops"] = fl["bwd"] / (statistics.median(bwd) * 1e-3) / 1e12
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -264,127 +417,35 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = wl.BY_NAME[args.workload]
-    inputs = wl.make_inputs(w)
-    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    es = 2 if w.dtype == "bf16" else 4
-
-    q8 = w.kv_format == "q8_0"
-    host = {n: torch.from_numpy(inputs[n]).to(dt).pin_memory() for n in (("q", "do") if q8 else ("q", "k", "v", "do"))}
-    if w.kv_format == "f16":   # an fp16 K/V cache, read in place (the library casts it for the tensor cores)
-        for n in ("k", "v"):
-            host[n] = torch.from_numpy(inputs[n]).to(torch.float16).pin_memory()
-    if q8:   # the K/V cache in its own format: int8 values and fp16 scales, read in place
-        for n in ("k", "v"):
-            qv, dv_ = inputs[n + "_q8"]
-            host[n + "_q"] = torch.from_numpy(qv).pin_memory()
-            host[n + "_d"] = torch.from_numpy(dv_).pin_memory()
-    if inputs["mask"] is not None:
-        host["mask"] = torch.from_numpy(inputs["mask"]).pin_memory()
-    d = {n: t.to(dev) for n, t in host.items()}
-    mask = d.get("mask")
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, window=w.window, deterministic=args.deterministic)
-    kv_format = {"q8_0": ft.FA_KV_Q8_0, "f16": ft.FA_KV_F16}.get(w.kv_format, ft.FA_KV_DTYPE)
-    p = ft.make_params(d["q"], d["k_q" if q8 else "k"], mask, kv_format=kv_format, **kw)
-    ws_f = torch.empty(max(ft.fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(max(ft.bwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
-    o = torch.empty_like(d["q"])
-    lse = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
-    dq = torch.empty_like(d["q"])
-    if w.accum:
-        dk = torch.from_numpy(inputs["dk_acc"]).to(dev)
-        dv = torch.from_numpy(inputs["dv_acc"]).to(dev)
-        # the chunk's own K/V rows (the last Sq keys of the window) are read back from the
-        # accumulator in the same kernel (fused SET_ROWS backward)
-        rows_shape = (w.B, w.Hkv, w.Sq, w.D)
-        dk_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
-        dv_rows = torch.empty(rows_shape, dtype=d["q"].dtype, device=dev)
-    else:
-        kv_shape = (w.B, w.Hkv, w.Sk, w.D)
-        dk, dv = torch.empty(kv_shape, dtype=dt, device=dev), torch.empty(kv_shape, dtype=dt, device=dev)
+    prep = Prepared(ft, torch, w, dev, deterministic=args.deterministic)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    fkw = {k_: v_ for k_, v_ in kw.items() if k_ != "deterministic"}
-
-    def fwd_call(src, o_, lse_):
-        if q8:
-            return ft.fwd_q8(src["q"], src["k_q"], src["k_d"], src["v_q"], src["v_d"], src.get("mask"), out=o_,
-                             lse=lse_, workspace=ws_f, **fkw)
-        return ft.fwd(src["q"], src["k"], src["v"], src.get("mask"), out=o_, lse=lse_, workspace=ws_f, **kw)
-
-    def bwd_call(src, o_, lse_, dq_, dk_, dv_):
-        if q8:
-            kv = (src["k_q"], src["k_d"], src["v_q"], src["v_d"])
-            if w.accum:
-                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk_acc=dk_, dv_acc=dv_,
-                          workspace=ws_b, **kw)
-            else:
-                ft.bwd_q8(src["q"], *kv, o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
-                          workspace=ws_b, **kw)
-        elif w.accum:
-            ft.bwd_accum_rows(src["q"], src["k"], src["v"], o_, lse_, src["do"], dk_, dv_, w.q_offset, w.Sq,
-                              src.get("mask"), dq=dq_, dk_rows=dk_rows, dv_rows=dv_rows, workspace=ws_b, **kw)
-        else:
-            ft.bwd(src["q"], src["k"], src["v"], o_, lse_, src["do"], src.get("mask"), dq=dq_, dk=dk_, dv=dv_,
-                   workspace=ws_b, **kw)
-
-    def step(src):
-        fwd_call(src, o, lse)
-        bwd_call(src, o, lse, dq, dk, dv)
-
     fl = wl.flops(w)
+    peaks = load_peaks()
+
     clocks = ClockSampler(local)
     clocks.start()
-    for _ in range(args.warmup):
-        step(d)
-    torch.cuda.synchronize()
-
     K = args.steps
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    step_ev = [(ev(), ev()) for _ in range(K)]
-    kern = {kid: [(ev(), ev()) for _ in range(K)] for kid in (ft.FA_KERNEL_FWD, ft.FA_KERNEL_BWD_MAIN,
-                                                              ft.FA_KERNEL_BWD_DSUM, ft.FA_KERNEL_BWD_DQ_CONVERT)}
-    # torch creates the CUDA event lazily at its first record(): materialise every handle
-    # before the library is asked to record it
-    for evs in kern.values():
-        for a_, b_ in evs:
-            a_.record()
-            b_.record()
     barrier(world)
     torch.cuda.synchronize()
-    launches0 = ft.profile_launch_count()
     t_wall = time.perf_counter()
-    for i in range(K):
-        flush.zero_()                      # evict L2 between timed steps (not inside the step events)
-        for kid, evs in kern.items():
-            ft.profile_set_events(kid, *evs[i])
-        step_ev[i][0].record()
-        step(d)
-        step_ev[i][1].record()
-    torch.cuda.synchronize()
+    step_ms, kern_ms, launches = timed_steps(torch, ft, prep, K, args.warmup, flush)
     barrier(world)
     t_wall = time.perf_counter() - t_wall
-    launches = ft.profile_launch_count() - launches0
-    for kid in kern:
-        ft.profile_set_events(kid, None, None)
     clock_info = clocks.stop()
 
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
-
-    def mean_or_zero(evs):
-        try:
-            return statistics.mean(a.elapsed_time(b) for a, b in evs)
-        except (RuntimeError, ValueError):  # this path does not launch that kernel
-            return 0.0
-
-    kern_ms = {kid: mean_or_zero(evs) for kid, evs in kern.items()}
     mean_ms, value = job_tflops(world, fl["total"], statistics.mean(step_ms))
 
-    peaks = load_peaks()
-    fwd_ms, bwd_main_ms = kern_ms[ft.FA_KERNEL_FWD], kern_ms[ft.FA_KERNEL_BWD_MAIN]
+    def mean_or_zero(v):
+        return statistics.mean(v) if v else 0.0
+
+    fwd_ms, bwd_main_ms = mean_or_zero(kern_ms["fwd"]), mean_or_zero(kern_ms["bwd_main"])
+    dsum_ms, dqconv_ms = mean_or_zero(kern_ms["bwd_dsum"]), mean_or_zero(kern_ms["bwd_dq_convert"])
     dominant = "bwd_main" if bwd_main_ms >= fwd_ms else "fwd"
     dom_ms = bwd_main_ms if dominant == "bwd_main" else fwd_ms
     dom_flops = fl["bwd"] if dominant == "bwd_main" else fl["fwd"]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     rows = w.B * w.Hq * w.Sq
+    es = prep.es
     dsum_bytes = rows * w.D * es * 2 + rows * 4 + rows * w.D * 4
     dqconv_bytes = rows * w.D * 4 + rows * w.D * es
     csrc = os.path.join(ROOT, "backward_adapter_gb300", "csrc")
@@ -392,19 +453,23 @@ def run_ours(args):
     traffic = measured_traffic(dominant, dom_src) if os.path.exists(dom_src) else None
 
     # End to end through the public API from pinned host buffers: every step copies its inputs
-    # host -> device and its results (dQ, dK, dV) device -> host. Copies run on a second stream
-    # into double-buffered device inputs, so step i+1's inputs arrive while step i computes.
-    out_host = [{"dq": torch.empty_like(dq, device="cpu").pin_memory(),
-                 "dk": torch.empty_like(dk, device="cpu").pin_memory(),
-                 "dv": torch.empty_like(dv, device="cpu").pin_memory()} for _ in range(2)]
+    # host -> device and its results (O, LSE, dQ, dK, dV) device -> host. Copies run on their
+    # own streams into double-buffered device buffers, so step i+1's inputs arrive while step i
+    # computes.
+    d, host = prep.d, prep.host
+    o, lse, dq, dk, dv = prep.o, prep.lse, prep.dq, prep.dk, prep.dv
+    out_host = [{n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
+                 (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host[0].values())
     bufs = [d, {n: torch.empty_like(t) for n, t in d.items()}]
-    outs = [(dq, dk, dv), (torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv))]
-    fwd_outs = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
+    outs = [(o, lse, dq, dk, dv),
+            (torch.empty_like(o), torch.empty_like(lse), torch.empty_like(dq), torch.empty_like(dk),
+             torch.empty_like(dv))]
     if w.accum:
-        outs[1][1].copy_(dk)
-        outs[1][2].copy_(dv)
+        outs[1][3].copy_(dk)
+        outs[1][4].copy_(dv)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     comp = torch.cuda.current_stream()
     copy = torch.cuda.Stream()        # host -> device
     copy_out = torch.cuda.Stream()    # device -> host (both directions at once)
@@ -429,15 +494,14 @@ def run_ours(args):
         if i >= 2:
             comp.wait_event(read_back[sl])          # step i-2's results have been read back
         src = bufs[sl]
-        o_, lse_ = fwd_call(src, fwd_outs[sl][0], fwd_outs[sl][1])
-        dq_, dk_, dv_ = outs[sl]
-        bwd_call(src, o_, lse_, dq_, dk_, dv_)
+        o_, lse_, dq_, dk_, dv_ = outs[sl]
+        prep.fwd_call(src, o_, lse_)
+        prep.bwd_call(src, o_, lse_, dq_, dk_, dv_)
         done[sl].record(comp)
         with torch.cuda.stream(copy_out):
             copy_out.wait_event(done[sl])
-            out_host[sl]["dq"].copy_(dq_, non_blocking=True)
-            out_host[sl]["dk"].copy_(dk_, non_blocking=True)
-            out_host[sl]["dv"].copy_(dv_, non_blocking=True)
+            for n, t in zip(("o", "lse", "dq", "dk", "dv"), outs[sl]):
+                out_host[sl][n].copy_(t, non_blocking=True)
             read_back[sl].record(copy_out)
     last = ev()
     last.record(copy_out)
@@ -447,27 +511,43 @@ def run_ours(args):
     barrier(world)
     e2e_ms, e2e_value = job_tflops(world, fl["total"], e0.elapsed_time(e1) / E)
 
+    # The other workloads of the op, each timed the same way (not part of the headline's timed
+    # region): rank 0 at N = 1 only, so the multi-GPU launch stays short.
+    by_workload = None
+    if rank == 0 and world == 1 and not args.no_by_workload:
+        by_workload = {}
+        for ow in wl.WORKLOADS:
+            if ow.name == w.name:
+                continue
+            op = Prepared(ft, torch, ow, dev)
+            s_ms, k_ms, _ = timed_steps(torch, ft, op, args.workload_steps, max(3, args.warmup), flush)
+            by_workload[ow.name] = workload_summary(ow, wl.flops(ow), s_ms, k_ms, peaks["bf16_tflops"])
+            del op
+        torch.cuda.synchronize()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # grow the sample one GQA group at a time until ~10 s of oracle work (or every head)
         G = w.Hq // w.Hkv
         heads = G
-        dt_cpu, fl_cpu, desc = oracle_sample(w, inputs, heads)
+        dt_cpu, fl_cpu, desc = oracle_sample(w, prep.inputs, heads)
         while dt_cpu < 10.0 and heads < w.Hq:
             heads = min(w.Hq, max(heads + G, int(heads * 10.0 / max(dt_cpu, 1e-3)) // G * G))
-            dt_cpu, fl_cpu, desc = oracle_sample(w, inputs, heads)
+            dt_cpu, fl_cpu, desc = oracle_sample(w, prep.inputs, heads)
         cpu = {"value": fl_cpu / dt_cpu / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc, "seconds": dt_cpu}
 
     if rank != 0:
         return 0
+    st = stats(step_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": mean_ms, "ms_per_step_median": st["median"], "ms_per_step_min": st["min"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "q_offset": w.q_offset, "window": w.window, "mask": w.mask, "accum": w.accum,
-                   "rows_read_back": [w.q_offset, w.Sq] if w.accum and not q8 else None,
+                   "rows_read_back": [w.q_offset, w.Sq] if w.accum and not prep.q8 else None,
                    "kv_format": w.kv_format,
                    "deterministic": bool(args.deterministic),
                    "visible_pairs": fl["pairs"], "gflop_per_step": fl["total"] / 1e9,
@@ -475,12 +555,12 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / peaks["bf16_tflops"],
         "fwd_tflops": fl["fwd"] / (fwd_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / ((bwd_main_ms + kern_ms[ft.FA_KERNEL_BWD_DSUM] +
-                                    kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]) * 1e-3) / 1e12,
-        "kernel_ms": {"fwd": fwd_ms, "bwd_main": bwd_main_ms, "bwd_dsum": kern_ms[ft.FA_KERNEL_BWD_DSUM],
-                      "bwd_dq_convert": kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]},
-        "hbm_passes_gbs": {"bwd_dsum": gbs(dsum_bytes, kern_ms[ft.FA_KERNEL_BWD_DSUM]),
-                           "bwd_dq_convert": gbs(dqconv_bytes, kern_ms[ft.FA_KERNEL_BWD_DQ_CONVERT]),
+        "bwd_tflops": fl["bwd"] / ((bwd_main_ms + dsum_ms + dqconv_ms) * 1e-3) / 1e12,
+        "kernel_ms": {"fwd": fwd_ms, "bwd_main": bwd_main_ms, "bwd_dsum": dsum_ms, "bwd_dq_convert": dqconv_ms},
+        "kernel_ms_median_min": {n: {"median": v["median"], "min": v["min"]}
+                                 for n, v in ((n, stats(x)) for n, x in kern_ms.items()) if v},
+        "hbm_passes_gbs": {"bwd_dsum": gbs(dsum_bytes, dsum_ms),
+                           "bwd_dq_convert": gbs(dqconv_bytes, dqconv_ms),
                            "peak": peaks["hbm_gbs"]},
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
@@ -488,10 +568,13 @@ def run_ours(args):
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "copies": "pinned host buffers; inputs and results on their own streams, double-buffered"},
+                "ms_per_step": e2e_ms,
+                "copies": "pinned host buffers; inputs and results (O, LSE, dQ, dK, dV) on their own streams, "
+                          "double-buffered"},
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
         "clocks": clock_info,
+        "by_workload": by_workload,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -277,7 +277,11 @@ FA_API uint64_t fa_profile_launch_count(void);
  * until the process exits. Shapes whose fa_train_bwd_workspace_size() exceeds 16 MiB are
  * rejected with FA_ERR_WORKSPACE (and a message in fa_last_error()) before anything runs.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, once
- * per device, with that device current); make that first call before any stream capture.
+ * per device, with that device current); make that first call before any stream capture. The
+ * address is kept for the life of the process: after cudaDeviceReset (or anything else that
+ * tears down and recreates the device's primary context) the array may move, and this entry
+ * point must not be called again in that process. The tensors and the stream must belong to
+ * the current device: the array is looked up, and the kernels launched, on that device.
  * The library allocates and frees nothing in this call. Every call shares the one array and
  * the kernels re-initialise what must start at zero, so back-to-back calls on one stream are
  * fine, but calls that overlap on the GPU (other streams, other host threads) race.

@@ -37,7 +37,15 @@ CASES = [
     wl.Workload("noalloc_causal_offset_d128", B=1, Hq=4, Hkv=2, Sq=700, Sk=900, D=128, causal=True, q_offset=200,
                 seed=41),
     wl.Workload("noalloc_bool_mask_d64", B=2, Hq=4, Hkv=1, Sq=300, Sk=260, D=64, mask="random_bool", seed=42),
+    # the fp32 path (SIMT kernels) and the ordered dQ adds (turn counters in the static array)
+    wl.Workload("noalloc_f32_causal_d64", B=1, Hq=4, Hkv=2, Sq=90, Sk=130, D=64, dtype="f32", causal=True,
+                q_offset=40, seed=43),
+    wl.Workload("noalloc_deterministic_causal_d128", B=1, Hq=4, Hkv=1, Sq=400, Sk=400, D=128, causal=True, seed=44),
 ]
+
+
+def _deterministic(w):
+    return w.name.startswith("noalloc_deterministic")
 
 
 @pytest.mark.gpu
@@ -49,8 +57,9 @@ def test_noalloc_backward_matches_workspace_backward_on_two_calls(w):
 
     inputs = wl.make_inputs(w)
     t = pu.to_device(inputs, w)
-    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
-    o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset, deterministic=_deterministic(w))
+    fkw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
+    o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **fkw)
     ref = ft.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], t["mask"], **kw)
     torch.cuda.synchronize()
     ref = [x.double().cpu().numpy() for x in ref]
@@ -61,6 +70,28 @@ def test_noalloc_backward_matches_workspace_backward_on_two_calls(w):
         assert ft.device_status() == 0
         for name, g, r in zip(("dq", "dk", "dv"), got, ref):
             g = g.double().cpu().numpy()
+            if _deterministic(w):
+                # same kernels, same ordered adds: the same bits as the workspace backward
+                assert np.array_equal(g, r), f"call {call}: deterministic {name} differs from the workspace backward"
             err = float(np.abs(g - r).max())
             bound = rel * float(np.abs(r).max()) + abs_
             assert err <= bound, f"call {call}: {name} differs from the workspace backward by {err:.3e} > {bound:.3e}"
+
+
+@pytest.mark.gpu
+def test_noalloc_backward_matches_the_oracle():
+    """One case compared with the fp64 oracle directly, not only with the workspace backward."""
+    import torch
+
+    from tests import parity_util as pu
+
+    w = CASES[0]
+    inputs = wl.make_inputs(w)
+    t = pu.to_device(inputs, w)
+    kw = dict(scale=w.scale, causal=w.causal, q_offset=w.q_offset)
+    o, lse = ft.fwd(t["q"], t["k"], t["v"], t["mask"], **kw)
+    dq, dk, dv = ft.bwd_noalloc(t["q"], t["k"], t["v"], o, lse, t["do"], t["mask"], **kw)
+    torch.cuda.synchronize()
+    assert ft.device_status() == 0
+    got = {n: x.double().cpu().numpy() for n, x in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    pu.assert_parity(w, got, pu.run_oracle(w, inputs))
