@@ -529,18 +529,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         uint32_t sr[32], dr[32];
         tmem_ld32(tb + c * 32, sr);
         if (cc > 0) tmem_ld32(tb + BQ + c * 32, dr);
+        // the chunk's 32 LSE values, loaded while the TMEM loads are in flight (the wait below
+        // orders every memory access, so loads issued after it would add their latency to it)
+        float l2c[32];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 a = ld_shared_f4(lse_s + (c * 32 + 4 * v4) * 4);
+          l2c[4 * v4] = a.x; l2c[4 * v4 + 1] = a.y; l2c[4 * v4 + 2] = a.z; l2c[4 * v4 + 3] = a.w;
+        }
         tmem_wait_ld();
         reg_fence(sr);
         float pv[32];
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           const int q0 = c * 32 + sub * 16;   // first query of these 16
-          float l2[16];
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float4 a = ld_shared_f4(lse_s + (q0 + 4 * v4) * 4);
-            l2[4 * v4] = a.x; l2[4 * v4 + 1] = a.y; l2[4 * v4 + 2] = a.z; l2[4 * v4 + 3] = a.w;
-          }
+          const float* l2 = l2c + sub * 16;
           float* pw = pv + sub * 16;
           if (full) {
 #pragma unroll
@@ -583,24 +586,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(pw[2 * e], pw[2 * e + 1]);
           tmem_st8(tb + c * 32 + sub * 8, pk);   // P^T of these 16 queries
         }
+        float dc[32];   // the chunk's 32 D values
         if (cc == 0) {
           // dP^T of the step (its MMAs ran under the exponentials above)
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdp_full[buf], (st / C::NBUF) & 1, abort_flag, p.status, 135));
           if (!ok) break;
           tc_fence_after();
           tmem_ld32(tb + BQ + c * 32, dr);
-          tmem_wait_ld();
         }
+        // loaded while the dP^T TMEM load is in flight (first round)
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 d = ld_shared_f4(lse_s + (BQ + c * 32 + 4 * v4) * 4);
+          dc[4 * v4] = d.x; dc[4 * v4 + 1] = d.y; dc[4 * v4 + 2] = d.z; dc[4 * v4 + 3] = d.w;
+        }
+        if (cc == 0) tmem_wait_ld();
         reg_fence(dr);
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
           const int q0 = c * 32 + sub * 16;
-          float dv_[16];
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float4 d = ld_shared_f4(lse_s + (BQ + q0 + 4 * v4) * 4);
-            dv_[4 * v4] = d.x; dv_[4 * v4 + 1] = d.y; dv_[4 * v4 + 2] = d.z; dv_[4 * v4 + 3] = d.w;
-          }
+          const float* dv_ = dc + sub * 16;
           const float* pw = pv + sub * 16;
           uint32_t dk8[8];
 #pragma unroll
