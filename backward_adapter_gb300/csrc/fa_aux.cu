@@ -105,26 +105,59 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }
 
 // One block per (mask batch, q-tile, k-tile) of 128 x 128, flattened in that order.
-__global__ void __launch_bounds__(256) mask_classify_kernel(Shape s, const void* __restrict__ mask,
+// One block per 128 x 128 tile. With vec (every row of the mask starts on a 16-byte boundary:
+// Sk % 4 == 0 for fp32, Sk % 16 == 0 for bytes) each thread reads 16-byte vectors, all of its loads
+// independent (a tile is 64 KB of fp32: latency, not bandwidth, sets the time); otherwise one
+// element at a time.
+template <bool ADD, bool VEC>
+__global__ void __launch_bounds__(512) mask_classify_kernel(Shape s, const void* __restrict__ mask,
                                                             uint8_t* __restrict__ tilemap, int nqt, int nkt) {
   const long long tile = blockIdx.x;
   const int kt = (int)(tile % nkt);
   const int qt = (int)((tile / nkt) % nqt);
   const int mb = (int)(tile / ((long long)nkt * nqt));
   bool any_vis = false, all_open = true;
-  for (int e = threadIdx.x; e < 128 * 128; e += 256) {
-    const int i = qt * 128 + e / 128, j = kt * 128 + e % 128;
-    if (i >= s.Sq || j >= s.Sk) continue;
-    const size_t idx = ((size_t)mb * s.Sq + i) * s.Sk + j;
-    if (s.mask_kind == MK_ADD) {
-      const float m = static_cast<const float*>(mask)[idx];
-      const bool vis = m > kMaskFloor;
-      any_vis |= vis;
-      all_open &= (m == 0.f);
-    } else {
-      const bool vis = static_cast<const uint8_t*>(mask)[idx] != 0;
-      any_vis |= vis;
-      all_open &= vis;
+  const int i0 = qt * 128, j0 = kt * 128;
+  constexpr int EPV = ADD ? 4 : 16;             // elements per 16-byte vector
+  constexpr int VPR = 128 / EPV;                // vectors per tile row
+  constexpr int PER_THREAD = 128 * VPR / 512;   // 8 (fp32) or 2 (bytes)
+  if (VEC) {
+#pragma unroll
+    for (int t = 0; t < PER_THREAD; ++t) {
+      const int v = t * 512 + (int)threadIdx.x;
+      const int i = i0 + v / VPR, j = j0 + (v % VPR) * EPV;
+      if (i >= s.Sq || j >= s.Sk) continue;   // rows and tails past the mask (Sk is a multiple of EPV)
+      const size_t idx = ((size_t)mb * s.Sq + i) * s.Sk + j;
+      if (ADD) {
+        const float4 m = *reinterpret_cast<const float4*>(static_cast<const float*>(mask) + idx);
+        any_vis |= (m.x > kMaskFloor) | (m.y > kMaskFloor) | (m.z > kMaskFloor) | (m.w > kMaskFloor);
+        all_open &= (m.x == 0.f) & (m.y == 0.f) & (m.z == 0.f) & (m.w == 0.f);
+      } else {
+        const uint4 m = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(mask) + idx);
+        const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          // a byte is visible when nonzero: some byte of w is visible iff w != 0, and
+          // (w - 0x01010101) & ~w & 0x80808080 is nonzero iff some byte of w is zero
+          any_vis |= w[u] != 0u;
+          all_open &= ((w[u] - 0x01010101u) & ~w[u] & 0x80808080u) == 0u;
+        }
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < 128 * 128; e += 512) {
+      const int i = i0 + e / 128, j = j0 + e % 128;
+      if (i >= s.Sq || j >= s.Sk) continue;
+      const size_t idx = ((size_t)mb * s.Sq + i) * s.Sk + j;
+      if (ADD) {
+        const float m = static_cast<const float*>(mask)[idx];
+        any_vis |= m > kMaskFloor;
+        all_open &= (m == 0.f);
+      } else {
+        const bool vis = static_cast<const uint8_t*>(mask)[idx] != 0;
+        any_vis |= vis;
+        all_open &= vis;
+      }
     }
   }
   any_vis = __syncthreads_or(any_vis);
@@ -187,7 +220,14 @@ cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tile
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = prof_begin(KID_MASK, st);
   if (e != cudaSuccess) return e;
-  mask_classify_kernel<<<(unsigned)tiles, 256, 0, st>>>(s, mask, tilemap, nqt, nkt);
+  const bool add = s.mask_kind == MK_ADD;
+  // rows start on 16-byte boundaries when Sk is a multiple of the vector width (the mask pointer
+  // itself is 16-byte aligned, checked by the entry points)
+  const bool vec = add ? (s.Sk % 4 == 0) : (s.Sk % 16 == 0);
+  if (add && vec) mask_classify_kernel<true, true><<<(unsigned)tiles, 512, 0, st>>>(s, mask, tilemap, nqt, nkt);
+  else if (add) mask_classify_kernel<true, false><<<(unsigned)tiles, 512, 0, st>>>(s, mask, tilemap, nqt, nkt);
+  else if (vec) mask_classify_kernel<false, true><<<(unsigned)tiles, 512, 0, st>>>(s, mask, tilemap, nqt, nkt);
+  else mask_classify_kernel<false, false><<<(unsigned)tiles, 512, 0, st>>>(s, mask, tilemap, nqt, nkt);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return prof_end(KID_MASK, st);
