@@ -79,29 +79,42 @@ __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, cons
   if (row < rows && part == 0) dsum[row] = acc;
 }
 
+// Each thread converts kConvVecs 8-element vectors, a grid stride apart, with all of their loads
+// issued before the first store (more bytes in flight per thread).
+constexpr int kConvVecs = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
                                                          float scale, long long vecs, int groups, const Shape s) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= vecs) return;
-  const long long e = i * 8;   // element of the accumulator, [B, Hq, Sq, D]
-  size_t at = (size_t)e;        // the same element of dQ when dQ is [B, Hq, Sq, D] too
-  if (s.layout) {
-    const long long row = e / s.D, bh = row / s.Sq, qi = row % s.Sq;
-    at = head_base(s, (int)(bh / s.Hq), (int)(bh % s.Hq), s.Hq, s.Sq) + (size_t)qi * row_stride(s, s.Hq) +
-         (size_t)(e % s.D);
-  }
-  float x[8];
-  load8(acc + i * 8, x);
-  for (int g = 1; g < groups; ++g) {   // the key-tile groups' accumulators, always in group order
-    float y[8];
-    load8(acc + ((long long)g * vecs + i) * 8, y);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  float x[kConvVecs][8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) x[t] += y[t];
+  for (int u = 0; u < kConvVecs; ++u) {
+    const long long i = i0 + u * stride;
+    if (i < vecs) load8(acc + i * 8, x[u]);
   }
 #pragma unroll
-  for (int t = 0; t < 8; ++t) x[t] *= scale;
-  store8(dq + at, x);
+  for (int u = 0; u < kConvVecs; ++u) {
+    const long long i = i0 + u * stride;
+    if (i >= vecs) break;
+    for (int g = 1; g < groups; ++g) {   // the key-tile groups' accumulators, always in group order
+      float y[8];
+      load8(acc + ((long long)g * vecs + i) * 8, y);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) x[u][t] += y[t];
+    }
+    const long long e = i * 8;   // element of the accumulator, [B, Hq, Sq, D]
+    size_t at = (size_t)e;        // the same element of dQ when dQ is [B, Hq, Sq, D] too
+    if (s.layout) {
+      const long long row = e / s.D, bh = row / s.Sq, qi = row % s.Sq;
+      at = head_base(s, (int)(bh / s.Hq), (int)(bh % s.Hq), s.Hq, s.Sq) + (size_t)qi * row_stride(s, s.Hq) +
+           (size_t)(e % s.D);
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) x[u][t] *= scale;
+    store8(dq + at, x[u]);
+  }
 }
 
 // One block per (mask batch, q-tile, k-tile) of 128 x 128, flattened in that order.
@@ -200,7 +213,7 @@ cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups)
   const Shape& s = a.s;
   const long long vecs = (long long)s.B * s.Hq * s.Sq * s.D / 8;
   if (vecs == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((vecs + 255) / 256);
+  const unsigned blocks = (unsigned)((vecs + 256LL * kConvVecs - 1) / (256LL * kConvVecs));
   cudaError_t e = prof_begin(KID_BWD_DQCONV, a.stream);
   if (e != cudaSuccess) return e;
   if (s.dtype == DT_BF16)
