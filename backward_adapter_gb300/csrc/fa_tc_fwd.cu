@@ -294,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       key_hi = min(key_hi, s.q_offset + i + s.window);
     }
     const size_t mrow = ((size_t)mb * s.Sq + (size_t)min(i, s.Sq - 1)) * (size_t)s.Sk;
+    // mask rows start on 16-byte boundaries (the mask pointer itself is 16-byte aligned)
+    const bool mask_vec = s.mask_kind == MK_ADD ? (s.Sk % 4 == 0) : (s.Sk % 16 == 0);
     float m = -CUDART_INF_F, l = 0.f;
     int idx = 0;
     bool ok = true;
@@ -328,19 +330,38 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           for (int e = 0; e < 32; ++e)
             x[c0 + e] = (c0 + e >= lo && c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         } else if (s.mask_kind == MK_ADD) {
-          // the row's 32 mask values first (independent loads), then the arithmetic
+          // the row's 32 mask values first (independent loads), then the arithmetic; 16-byte loads
+          // when the chunk lies inside the row's visible keys and mask rows are 16-byte aligned
           const float* mp = static_cast<const float*>(p.mask) + mrow + key0 + c0;
           float mv[32];
+          if (mask_vec && c0 >= lo && c0 + 31 <= lim) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mv[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
+            for (int v4 = 0; v4 < 8; ++v4) {
+              const float4 m4 = __ldg(reinterpret_cast<const float4*>(mp) + v4);
+              mv[4 * v4] = m4.x; mv[4 * v4 + 1] = m4.y; mv[4 * v4 + 2] = m4.z; mv[4 * v4 + 3] = m4.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mv[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : -CUDART_INF_F;
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             x[c0 + e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
         } else {
           const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + mrow + key0 + c0;
           uint32_t mb8[32];
+          if (mask_vec && c0 >= lo && c0 + 31 <= lim) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : 0u;
+            for (int v = 0; v < 2; ++v) {
+              const uint4 m16 = __ldg(reinterpret_cast<const uint4*>(mp) + v);
+              const uint32_t w[4] = {m16.x, m16.y, m16.z, m16.w};
+#pragma unroll
+              for (int e = 0; e < 16; ++e) mb8[16 * v + e] = (w[e / 4] >> (8 * (e % 4))) & 0xffu;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : 0u;
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c0 + e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
         }
