@@ -175,7 +175,10 @@ __device__ __forceinline__ int bwd_tile_code(const BwdTcParams& p, int mb, int i
   return p.tilemap[((size_t)mb * p.nqt + i0 / 128) * p.nkt + kt];
 }
 
-template <int D>
+// MASKED: the call has a mask tensor. Without one no tile is mixed, and that instance has no
+// mixed-tile code at all: the softmax-grad loop's unrolled variants compete for the instruction
+// cache with every other role's loop, and the unused one cost 3% of the causal backward.
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const int base = it.i0 + q0;
             const int rlo = (int)max(0LL, min(row_lo - base, 16LL));
             const int rhi = key_ok && code != TILE_SKIP ? (int)max(0LL, min(row_hi - base + 1, 16LL)) : 0;
-            if (code != TILE_MIXED) {
+            if (!MASKED || code != TILE_MIXED) {
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 pw[e] = (e >= rlo && e < rhi) ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e])) : 0.f;
@@ -1067,12 +1070,13 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   p.part = split.n_units > 0 ? reinterpret_cast<float*>(ws + plan.part_off) : nullptr;
   memcpy(p.units, split.units, sizeof(uint32_t) * split.n_units);
   const int smem = C::BYTES;
-  if ((e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  auto kernel = s.mask_kind != MK_NONE ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const long long ctas = (long long)s.B * s.Hkv * (split.n_units > 0 ? split.n_units : p.nkt);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if ((e = prof_begin(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
-  bwd_tc_kernel<D><<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
+  kernel<<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (split.n_units > 0) {

@@ -109,7 +109,8 @@ __device__ __forceinline__ bool skip_tile(const FwdTcParams& p, int mb, int qt0,
   return tile_code(p, mb, qt0, j) == TILE_SKIP && tile_code(p, mb, qt0 + 1, j) == TILE_SKIP;
 }
 
-template <int D>
+// MASKED: the call has a mask tensor (without one, the instance has no mixed-tile code).
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdTcParams p) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         } else if (dead) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c0 + e] = -CUDART_INF_F;
-        } else if (code != TILE_MIXED) {
+        } else if (!MASKED || code != TILE_MIXED) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             x[c0 + e] = (c0 + e >= lo && c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
@@ -634,11 +635,12 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   p.n_qpairs = n_qpairs(s);
   p.status = status;
   const int smem = FwdSmem<D>::kBytes;
-  if ((e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  auto kernel = s.mask_kind != MK_NONE ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const long long ctas = (long long)s.B * s.Hq * p.n_qpairs * plan.kv_splits;
   if ((e = prof_begin(KID_FWD, a.stream)) != cudaSuccess) return e;
-  fwd_tc_kernel<D><<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
+  kernel<<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (plan.kv_splits > 1) {
