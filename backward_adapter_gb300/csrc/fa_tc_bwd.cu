@@ -548,20 +548,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           const int q0 = c * 32 + sub * 16;   // first query of these 16
           const float* l2 = l2c + sub * 16;
           float* pw = pv + sub * 16;
-          if (full) {
+          if (!MASKED || full || code != TILE_MIXED) {
+            // full and partial tiles share the exponentials (one copy of the unrolled loop: code
+            // size matters here); a partial tile then zeroes the query rows outside this key's
+            // visible rows [rlo, rhi) (causal rule, window, query tail), a 16-bit set
 #pragma unroll
             for (int e = 0; e < 16; ++e) pw[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
+            if (!full) {
+              const int base = it.i0 + q0;
+              const int rlo = (int)max(0LL, min(row_lo - base, 16LL));
+              const int rhi = key_ok && code != TILE_SKIP ? (int)max(0LL, min(row_hi - base + 1, 16LL)) : 0;
+              const uint32_t vis = rhi > rlo ? ((1u << rhi) - 1u) & ~((1u << rlo) - 1u) : 0u;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pw[e] = (vis >> e) & 1u ? pw[e] : 0.f;
+            }
           } else {
-            // visible query rows of this key are [rlo, rhi) relative to base (causal rule, window,
-            // query tail); rhi <= rlo when none is
+            // a mixed tile: visible query rows of this key are [rlo, rhi) relative to base (causal
+            // rule, window, query tail), and the mask decides within them
             const int base = it.i0 + q0;
             const int rlo = (int)max(0LL, min(row_lo - base, 16LL));
-            const int rhi = key_ok && code != TILE_SKIP ? (int)max(0LL, min(row_hi - base + 1, 16LL)) : 0;
-            if (!MASKED || code != TILE_MIXED) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                pw[e] = (e >= rlo && e < rhi) ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e])) : 0.f;
-            } else {
+            const int rhi = key_ok ? (int)max(0LL, min(row_hi - base + 1, 16LL)) : 0;
+            {
               // the 16 mask values of this key (one per query row) first, then the arithmetic
               float bias[16];
               if (s.mask_kind == MK_ADD) {

@@ -320,16 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       // the whole score row of this tile in registers (one TMEM wait), masked and scaled in place
       float x[kBN];
       auto masked = [&](const uint32_t (&raw)[32], int c0) {
-        if (full) {
+        if (!MASKED || full || dead || code != TILE_MIXED) {
+          // full, dead and partial tiles share one copy of the unrolled scaling (code size matters
+          // here); a dead or partial tile then hides the keys outside [lo, lim] of this 32-key chunk
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c0 + e] = __uint_as_float(raw[e]) * sl2;
-        } else if (dead) {
+          if (!full) {
+            const int a = max(lo - c0, 0), z = min(lim - c0 + 1, 32);
+            const uint32_t vis = (dead || z <= a) ? 0u : (uint32_t)(((1ull << z) - 1ull) & ~((1ull << a) - 1ull));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c0 + e] = -CUDART_INF_F;
-        } else if (!MASKED || code != TILE_MIXED) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            x[c0 + e] = (c0 + e >= lo && c0 + e <= lim) ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+            for (int e = 0; e < 32; ++e) x[c0 + e] = (vis >> e) & 1u ? x[c0 + e] : -CUDART_INF_F;
+          }
         } else if (s.mask_kind == MK_ADD) {
           // the row's 32 mask values first (independent loads), then the arithmetic; 16-byte loads
           // when the chunk lies inside the row's visible keys and mask rows are 16-byte aligned
