@@ -239,6 +239,9 @@ BwdPlan plan_bwd(const Shape& s) {
       p.part_off = off;
       p.part_bytes = (size_t)s.B * s.Hkv * split.n_slots * 2 * 128 * s.D * 4;
       off = align_up(off + p.part_bytes);
+      p.cnt_off = off;
+      p.cnt_bytes = (size_t)s.B * s.Hkv * split.n_slots * 2 * 4;
+      off = align_up(off + p.cnt_bytes);
     }
     if (s.kv_format == FA_KV_F16) {
       p.kvbf_off = off;
@@ -506,6 +509,22 @@ fa_status fa_set_rows_backward(const float* acc, int32_t B, int32_t H, int32_t S
   return cuda_status(launch_set_rows_backward(acc, (int)heads, S, D, idx, n_rows, out, out_dtype,
                                               device_status_ptr(), (cudaStream_t)stream),
                      "set_rows backward launch");
+}
+
+fa_status fa_train_bwd_plan(const fa_params* p, int32_t* records, int32_t cap, int32_t* n_ctas) {
+  Shape s;
+  fa_status st = check_params(p, s);
+  if (st != FA_OK) return st;
+  if (n_ctas == nullptr || cap < 0 || (cap > 0 && records == nullptr)) {
+    set_error("n_ctas must be non-null, cap >= 0, records non-null when cap > 0");
+    return FA_ERR_INVALID_ARG;
+  }
+  if (!plan_bwd(s).tensor_core) {
+    set_error("this backward does not take the tensor-core path");
+    return FA_ERR_UNSUPPORTED;
+  }
+  *n_ctas = bwd_plan_records(s, records, cap);
+  return FA_OK;
 }
 
 fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream) {

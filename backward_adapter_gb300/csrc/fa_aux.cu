@@ -8,6 +8,8 @@
 //     in the hot loop) or mixed.
 // Each thread moves 16-byte vectors; rows are split across 8..16 lanes. The file also holds
 // the self-test of the kernels' bounded waits.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -52,9 +54,11 @@ __device__ __forceinline__ void store8(float* p, const float* x) {
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dsum_kernel(const T* __restrict__ o, const T* __restrict__ dO,
                                                    float* __restrict__ dsum, float* __restrict__ dq_acc,
-                                                   long long rows, int groups, const Shape s) {
+                                                   long long rows, int groups, uint32_t* __restrict__ zero_words,
+                                                   int n_zero, const Shape s) {
   constexpr int LPR = D / 8;  // lanes per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid < n_zero) zero_words[tid] = 0u;
   const long long row = tid / LPR;   // over [B, Hq, Sq], like D and the dQ accumulators
   const int part = (int)(tid % LPR);
   float acc = 0.f;
@@ -181,28 +185,31 @@ __global__ void __launch_bounds__(512) mask_classify_kernel(Shape s, const void*
 
 }  // namespace
 
-cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups) {
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups, uint32_t* zero_words,
+                        int n_zero) {
   const Shape& s = a.s;
   const long long rows = (long long)s.B * s.Hq * s.Sq;
-  if (rows == 0) return cudaSuccess;
-  const long long threads = rows * (s.D / 8);
+  if (rows == 0 && n_zero == 0) return cudaSuccess;
+  const long long threads = std::max<long long>(rows * (s.D / 8), n_zero);
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   cudaError_t e = prof_begin(KID_BWD_DSUM, a.stream);
   if (e != cudaSuccess) return e;
   if (s.dtype == DT_BF16) {
     if (s.D == 64)
       dsum_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, s);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, zero_words,
+          n_zero, s);
     else
       dsum_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(
-          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, s);
+          (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, dsum, dq_acc_to_zero, rows, groups, zero_words,
+          n_zero, s);
   } else {
     if (s.D == 64)
       dsum_kernel<float, 64><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                           dq_acc_to_zero, rows, groups, s);
+                                                           dq_acc_to_zero, rows, groups, zero_words, n_zero, s);
     else
       dsum_kernel<float, 128><<<blocks, 256, 0, a.stream>>>((const float*)a.o, (const float*)a.dO, dsum,
-                                                            dq_acc_to_zero, rows, groups, s);
+                                                            dq_acc_to_zero, rows, groups, zero_words, n_zero, s);
   }
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

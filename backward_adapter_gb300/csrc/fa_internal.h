@@ -92,7 +92,8 @@ struct BwdPlan {
   size_t dsum_off, dsum_bytes;   // fp32 [B, Hq, Sq]
   size_t dqacc_off, dqacc_bytes; // fp32 [groups, B, Hq, Sq, D]
   size_t turn_off, turn_bytes;   // deterministic: int32 [groups, B, Hq, ceil(Sq / 128)] dQ turn counters
-  size_t part_off, part_bytes;   // split key tiles: fp32 dK/dV partials [B * Hkv, slots, 2, 128, D]
+  size_t part_off, part_bytes;   // split key tiles: fp32 dV/dK partials [B * Hkv, slots, 2, D / 4, 128] float4
+  size_t cnt_off, cnt_bytes;     // split key tiles: int32 [B * Hkv, slots, 2] part tickets / partials written
   size_t kvbf_off, kvbf_bytes;   // f16 cache: bf16 K then V, in the call's layout
   size_t total;
 };
@@ -120,19 +121,30 @@ void count_launches(int n);
 constexpr int kDetGroup = 8;
 inline int dq_groups(const Shape& s) { return s.deterministic ? ((s.Sk + 127) / 128 + kDetGroup - 1) / kDetGroup : 1; }
 
-// Backward work split (tensor-core path): a key tile whose query range is much longer than the
-// per-SM average share is split into up to kMaxParts parts, each a CTA of its own that writes fp32
-// dK/dV partials, summed afterwards in part order. Units run heaviest first.
+// Backward work split (tensor-core path). A key tile's query steps may be cut into up to kMaxParts
+// parts (consecutive query tiles), each a CTA of its own that writes fp32 dK/dV partials; the
+// part that finishes last sums all of them in part order and writes dK/dV. Two cases:
+//  - the key tiles of all (batch, key/value head) pairs are fewer than the SMs: key tiles well
+//    above the per-SM share are cut into even parts, units run heaviest first;
+//  - a full grid whose heaviest key tiles are longer than the per-SM share (the causal rule): the
+//    heavy tiles shed their last query tiles into a second part, and the CTAs are packed onto the
+//    SMs ahead of time (best-fit decreasing on a cost per step and per CTA); the launch order is
+//    the packing's planned start order, so the block scheduler, which hands the next block to the
+//    first SM that frees up, reproduces it.
 constexpr int kMaxUnits = 512;
 constexpr int kMaxParts = 8;
+constexpr int kMaxCtas = 1024;
 struct BwdSplit {
   int n_units = 0;        // 0: no split, one CTA per key tile in key-tile order
   int n_slots = 0;        // partial slots per (batch, key/value head)
-  int n_split = 0;        // key tiles that are split
-  uint32_t units[kMaxUnits];   // kt | part << 12 | nparts << 16 | slot << 20, heaviest first
-  uint32_t split[kMaxUnits];   // kt | nparts << 12 | first slot << 16, for the partial sum
+  int n_ctas = 0;         // 0: CTA i runs unit i / (B * Hkv) for (batch, kv head) i % (B * Hkv)
+  uint32_t units[kMaxUnits];   // kt | part << 12 | nparts << 16 | slot << 20
+  uint32_t range[kMaxUnits];   // the part's query tiles, from the key tile's first: first | end << 16
+  uint32_t ctas[kMaxCtas];     // launch order: unit | (batch * Hkv + kv head) << 16
 };
 void plan_bwd_split(const Shape& s, BwdSplit& out);
+// The plan as records (see fa_train_bwd_plan): returns the CTA count, writes at most `cap` records.
+int bwd_plan_records(const Shape& s, int32_t* rec, int cap);
 
 FwdPlan plan_fwd(const Shape& s);
 BwdPlan plan_bwd(const Shape& s);
@@ -142,9 +154,10 @@ cudaError_t simt_fwd(const FwdArgs& a);
 cudaError_t simt_bwd(const BwdArgs& a, float* dsum);
 
 // Helper passes shared by both paths.
-// dsum also zeroes `groups` fp32 dQ accumulators (none when dq_acc_to_zero is null); dq_convert
-// sums the groups in order, scales and converts to the dtype.
-cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups = 1);
+// dsum also zeroes `groups` fp32 dQ accumulators (none when dq_acc_to_zero is null) and n_zero
+// words at zero_words; dq_convert sums the groups in order, scales and converts to the dtype.
+cudaError_t launch_dsum(const BwdArgs& a, float* dsum, float* dq_acc_to_zero, int groups = 1,
+                        uint32_t* zero_words = nullptr, int n_zero = 0);
 cudaError_t launch_dq_convert(const BwdArgs& a, const float* dq_acc, int groups = 1);
 cudaError_t launch_mask_classify(const Shape& s, const void* mask, uint8_t* tilemap, cudaStream_t st);
 

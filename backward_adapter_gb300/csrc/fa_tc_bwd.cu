@@ -37,6 +37,11 @@
 #include <cstring>
 #include <cmath>
 #include <algorithm>
+#include <climits>
+#include <functional>
+#include <queue>
+#include <set>
+#include <vector>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -127,9 +132,12 @@ struct BwdTcParams {
   int nqt, nkt;
   unsigned* status;
   // work units (see BwdSplit): n_units == 0 runs one CTA per key tile in key-tile order
-  int n_units, n_slots;
-  float* part;                  // fp32 dK/dV partials of split key tiles [B * Hkv, n_slots, 2, 128, D]
+  int n_units, n_slots, n_ctas;
+  float* part;                  // fp32 dV/dK partials of split key tiles [B * Hkv, n_slots, 2, D / 4, 128] float4
+  int* part_sync;               // per (batch, kv head, first slot of a split key tile): tickets, partials written
   uint32_t units[kMaxUnits];    // kt | part << 12 | nparts << 16 | slot << 20
+  uint32_t range[kMaxUnits];    // a part's query tiles from the key tile's first: first | end << 16
+  uint32_t ctas[kMaxCtas];      // n_ctas > 0: CTA i runs unit ctas[i] & 0xffff of (batch, kv head) ctas[i] >> 16
 };
 
 // Query rows [ibeg, iend) that can see a key of tile kt, from the causal rule and the window, with
@@ -205,6 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   uint64_t* bar_s_full = bar_stage_full + 1;            // NBUF: S^T of the block is in TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s_full + C::NBUF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_part = abort_flag + 1;   // split key tile: this CTA's part finished last
+  volatile int* parts_ready = abort_flag + 2; // ... and the other parts' partials are written
   float* lsed = reinterpret_cast<float*>(smem + C::OFF_LSED);
 
   const Shape& s = p.s;
@@ -216,26 +226,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   //      light ones fill the SMs that free up (longest work first)
   //      A split key tile's parts each take a consecutive share of its query tiles.
   const int nbkv = s.B * s.Hkv;
-  int kt = blockIdx.x / nbkv, part = 0, nparts = 1, slot = 0;
+  int unit = blockIdx.x / nbkv, bkv = blockIdx.x % nbkv;
+  if (p.n_ctas > 0) {   // the planned launch order
+    const uint32_t c = p.ctas[blockIdx.x];
+    unit = (int)(c & 0xffffu);
+    bkv = (int)(c >> 16);
+  }
+  int kt = unit, part = 0, nparts = 1, slot = 0;
+  uint32_t range = 0;
   if (p.n_units > 0) {
-    const uint32_t u = p.units[blockIdx.x / nbkv];
+    const uint32_t u = p.units[unit];
     kt = (int)(u & 0xfffu);
     part = (int)((u >> 12) & 0xfu);
     nparts = (int)((u >> 16) & 0xfu);
     slot = (int)(u >> 20);
+    range = p.range[unit];
   }
-  const int bkv = blockIdx.x % nbkv;
   const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
   const int j0 = kt * kBN;
   const int mb = s.mask_batch > 1 ? b : 0;
   int ibeg, iend;
   key_tile_rows(s, kt, BQ, ibeg, iend);
-  if (nparts > 1) {
-    const int tiles = (iend - ibeg + BQ - 1) / BQ;
-    const int t0 = part * tiles / nparts, t1 = (part + 1) * tiles / nparts;
+  if (nparts > 1) {   // the part's own query tiles
     const int base = ibeg;
-    ibeg = base + t0 * BQ;
-    iend = min(iend, base + t1 * BQ);
+    ibeg = base + (int)(range & 0xffffu) * BQ;
+    iend = min(iend, base + (int)(range >> 16) * BQ);
   }
 
   if (threadIdx.x == 0) {
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // key's row band (which also ends at the last real row)
       const bool full = code == TILE_OPEN && key_ok && it.i0 >= row_lo && (long long)it.i0 + BQ - 1 <= row_hi;
       const uint32_t sds = smem_u32(smem + C::OFF_DS + dsb * C::DS_TILE) + r * 128;
-#pragma unroll
+#pragma unroll 1   // one copy of the round body: the hot loop's code stays small
       for (int cc = 0; cc < C::CHUNKS_PER_WARP; ++cc) {
         // round cc covers queries [64cc, 64cc + 64): the two warps of a lane quadrant take one
         // 32-query chunk each, and the first round is handed to the dV / dK MMAs right away
@@ -658,90 +673,139 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     ok = __all_sync(0xffffffffu, ok);
     if (ok && st > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma_done, 0, abort_flag, p.status, 133));
     tc_fence_after();
-    if (ok && nparts > 1) {
-      // a part of a split key tile: its fp32 sums (dK scaled) go to the partial slot, summed later
+    // One 32-feature chunk of dV (which = 0) or dK (which = 1) of this thread's key, already scaled,
+    // to its destination: the bf16 rows, or the fp32 accumulator (and the read-back rows).
+    const size_t row = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)(key_ok ? j : 0) * row_stride(s, s.Hkv);
+    // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
+    const long long rr = (long long)j - p.rows_begin;
+    const bool read_back = p.accum && key_ok && rr >= 0 && rr < p.n_rows;
+    const size_t rrow = head_base(s, b, kvh, s.Hkv, p.n_rows) + (size_t)(read_back ? rr : 0) * row_stride(s, s.Hkv);
+    auto store_chunk = [&](int which, int c, const float* x) {
+      if (!key_ok) return;
+      void* outp = which == 0 ? p.dv : p.dk;
+      if (p.accum) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(outp) + row + c * 32);
+        // all eight loads first (the read-back stores below could alias them as far as the
+        // compiler knows), then the adds and the stores
+        float4 a[8];
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float mul = which == 0 ? 1.f : s.scale;
-        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
-        float* dst = p.part + ((((size_t)bkv * p.n_slots + slot) * 2 + which) * kBN + r) * D;
+        for (int v4 = 0; v4 < 8; ++v4) a[v4] = dst[v4];
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          const int c = half * (D / 64) + cc;      // 32-feature chunk
-          uint32_t v[32];
-          if (st > 0) {
-            tmem_ld32(tcol + c * 32, v);
-            tmem_wait_ld();
-            reg_fence(v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0u;
-          }
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+        for (int v4 = 0; v4 < 8; ++v4) {
+          a[v4].x += x[4 * v4];
+          a[v4].y += x[4 * v4 + 1];
+          a[v4].z += x[4 * v4 + 2];
+          a[v4].w += x[4 * v4 + 3];
+          dst[v4] = a[v4];
+        }
+        if (read_back) {
+          uint2* rdst = reinterpret_cast<uint2*>((which == 0 ? p.dv_rows : p.dk_rows) + rrow + c * 32);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
-            d4[v4] = make_float4(__uint_as_float(v[4 * v4]) * mul, __uint_as_float(v[4 * v4 + 1]) * mul,
-                                 __uint_as_float(v[4 * v4 + 2]) * mul, __uint_as_float(v[4 * v4 + 3]) * mul);
+            rdst[v4] = make_uint2(pack_bf16x2(a[v4].x, a[v4].y), pack_bf16x2(a[v4].z, a[v4].w));
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outp) + row + c * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) w[u] = pack_bf16x2(x[8 * v4 + 2 * u], x[8 * v4 + 2 * u + 1]);
+          dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    };
+    // this thread's sums of one chunk from TMEM, scaled (zero when the CTA had no step)
+    auto load_chunk = [&](int which, int c, float* x) {
+      const float mul = which == 0 ? 1.f : s.scale;
+      const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
+      uint32_t v[32];
+      if (st > 0) {
+        tmem_ld32(tcol + c * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]) * mul;
+    };
+    if (nparts > 1) {
+      // A part of a split key tile. A ticket per key tile tells the part that finishes last: every
+      // other part writes its fp32 sums to its partial slot and counts itself written; the last
+      // one waits for those writes, adds the slots and its own sums (from TMEM) in part order and
+      // writes dK / dV. All eight warps reach the barriers below whatever `ok` says.
+      const size_t slot0 = (size_t)bkv * p.n_slots + (slot - part);
+      int* sync = p.part_sync + 2 * slot0;   // [tickets taken, partials written]
+      if (warp == 4 && lane == 0) *last_part = atom_add_acq_rel_gpu(sync, 1) == nparts - 1 ? 1 : 0;
+      named_bar_sync(1, 256);
+      if (*last_part == 0) {
+        if (ok) {
+          // a slot is [dV, dK] x [D / 4][128 keys] float4: a warp's 32 keys move 512 contiguous bytes
+          float4* mine = reinterpret_cast<float4*>(p.part + ((size_t)bkv * p.n_slots + slot) * 2 * kBN * D) + r;
+#pragma unroll
+          for (int which = 0; which < 2; ++which)
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+              const int c = half * (D / 64) + cc;      // 32-feature chunk
+              float x[32];
+              load_chunk(which, c, x);
+              float4* d4 = mine + ((size_t)which * (D / 4) + c * 8) * kBN;
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                d4[v4 * kBN] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
+            }
+        }
+        __threadfence();
+        named_bar_sync(1, 256);
+        if (warp == 4 && lane == 0) red_release_gpu_add(sync + 1, 1);
+      } else {
+        if (warp == 4 && lane == 0) *parts_ready = wait_turn(sync + 1, nparts - 1, abort_flag, p.status, 137) ? 1 : 0;
+        named_bar_sync(1, 256);
+        if (ok && *parts_ready) {
+          fence_acq_rel_gpu();
+          const float4* slots = reinterpret_cast<const float4*>(p.part + slot0 * 2 * kBN * D) + r;
+#pragma unroll
+          for (int which = 0; which < 2; ++which)
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+              const int c = half * (D / 64) + cc;
+              float x[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) x[e] = 0.f;
+              for (int q = 0; q < nparts; ++q) {
+                float y[32];
+                if (q == part) {
+                  load_chunk(which, c, y);
+                } else {
+                  const float4* src = slots + (((size_t)q * 2 + which) * (D / 4) + c * 8) * kBN;
+#pragma unroll
+                  for (int v4 = 0; v4 < 8; ++v4) {
+                    const float4 v = __ldcg(src + v4 * kBN);
+                    y[4 * v4] = v.x;
+                    y[4 * v4 + 1] = v.y;
+                    y[4 * v4 + 2] = v.z;
+                    y[4 * v4 + 3] = v.w;
+                  }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] += y[e];
+              }
+              store_chunk(which, c, x);
+            }
         }
       }
     } else if (ok) {
-      const size_t row = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)(key_ok ? j : 0) * row_stride(s, s.Hkv);
-      // the fused SET_ROWS backward: this key's finished sum is also one of the read-back rows
-      const long long rr = (long long)j - p.rows_begin;
-      const bool read_back = p.accum && key_ok && rr >= 0 && rr < p.n_rows;
-      const size_t rrow = head_base(s, b, kvh, s.Hkv, p.n_rows) + (size_t)(read_back ? rr : 0) * row_stride(s, s.Hkv);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float mul = which == 0 ? 1.f : s.scale;
-        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::DV_COL : C::DK_COL);
-        void* outp = which == 0 ? p.dv : p.dk;
+      for (int which = 0; which < 2; ++which)
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
           const int c = half * (D / 64) + cc;      // 32-feature chunk
-          uint32_t v[32];
-          if (st > 0) {
-            tmem_ld32(tcol + c * 32, v);
-            tmem_wait_ld();
-            reg_fence(v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0u;
-          }
-          if (!key_ok) continue;
-          if (p.accum) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(outp) + row + c * 32);
-            // all eight loads first (the read-back stores below could alias them as far as the
-            // compiler knows), then the adds and the stores
-            float4 a[8];
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) a[v4] = dst[v4];
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-              a[v4].x += __uint_as_float(v[4 * v4]) * mul;
-              a[v4].y += __uint_as_float(v[4 * v4 + 1]) * mul;
-              a[v4].z += __uint_as_float(v[4 * v4 + 2]) * mul;
-              a[v4].w += __uint_as_float(v[4 * v4 + 3]) * mul;
-              dst[v4] = a[v4];
-            }
-            if (read_back) {
-              uint2* rdst = reinterpret_cast<uint2*>((which == 0 ? p.dv_rows : p.dk_rows) + rrow + c * 32);
-#pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4)
-                rdst[v4] = make_uint2(pack_bf16x2(a[v4].x, a[v4].y), pack_bf16x2(a[v4].z, a[v4].w));
-            }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outp) + row + c * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint32_t w[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                w[u] = pack_bf16x2(__uint_as_float(v[8 * v4 + 2 * u]) * mul, __uint_as_float(v[8 * v4 + 2 * u + 1]) * mul);
-              dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
+          float x[32];
+          load_chunk(which, c, x);
+          store_chunk(which, c, x);
         }
-      }
     }
   } else {
     regs_inc<kRegsStager>();
@@ -892,82 +956,167 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
-// The parts of split key tiles, summed in part order: each thread takes 4 features of one key row,
-// for dK and dV, and writes them like the main kernel's epilogue would have.
-struct SplitReduceParams {
-  Shape s;
-  const float* part;
-  void* dk;
-  void* dv;
-  int accum;
-  long long rows_begin;
-  int n_rows;
-  __nv_bfloat16* dk_rows;
-  __nv_bfloat16* dv_rows;
-  int n_slots, n_split;
-  uint32_t split[kMaxUnits];   // kt | nparts << 12 | first slot << 16
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) bwd_split_reduce_kernel(const __grid_constant__ SplitReduceParams p) {
-  const Shape& s = p.s;
-  constexpr int V = D / 4;
-  const int nbkv = s.B * s.Hkv;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)p.n_split * nbkv * kBN * V) return;
-  const int c4 = (int)(idx % V);
-  const int r = (int)((idx / V) % kBN);
-  const long long rest = idx / ((long long)V * kBN);
-  const int bkv = (int)(rest % nbkv), si = (int)(rest / nbkv);
-  const uint32_t u = p.split[si];
-  const int kt = (int)(u & 0xfffu), np = (int)((u >> 12) & 0xfu), slot0 = (int)(u >> 16);
-  const int j = kt * kBN + r;
-  if (j >= s.Sk) return;
-  const int b = bkv / s.Hkv, kvh = bkv % s.Hkv;
-  const size_t out = head_base(s, b, kvh, s.Hkv, s.Sk) + (size_t)j * row_stride(s, s.Hkv) + 4 * c4;
-  const long long rr = (long long)j - p.rows_begin;
-  const bool read_back = p.accum && rr >= 0 && rr < p.n_rows;
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < np; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(
-          p.part + ((((size_t)bkv * p.n_slots + slot0 + q) * 2 + which) * kBN + r) * D + 4 * c4);
-      a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-    }
-    void* dst = which == 0 ? p.dv : p.dk;
-    if (p.accum) {
-      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + out);
-      float4 o = *d;
-      o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
-      *d = o;
-      if (read_back) {
-        __nv_bfloat16* rows = which == 0 ? p.dv_rows : p.dk_rows;
-        *reinterpret_cast<uint2*>(rows + head_base(s, b, kvh, s.Hkv, p.n_rows) + (size_t)rr * row_stride(s, s.Hkv) +
-                                  4 * c4) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
-      }
-    } else {
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dst) + out) =
-          make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
-    }
-  }
-}
-
 }  // namespace
 
 bool tc_bwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq > 0; }
 
-void plan_bwd_split(const Shape& s, BwdSplit& out) {
-  out.n_units = out.n_slots = out.n_split = 0;
-  constexpr int kSms = 152;
+namespace {
+
+// Cost of a CTA in query-tile steps (one step: the five 128 x 128 x D products of a query tile):
+// its steps, a fixed cost per CTA (TMEM and barriers, the K / V tiles, filling and draining the
+// pipeline, dK / dV out of TMEM) and, for a part of a split key tile, the round trip of its fp32
+// partial. Measured per CTA on the causal backward over 4096 keys: about 3.1 us a step, 10 us a
+// CTA and 2 us a part.
+constexpr double kCtaCost = 3.2, kPartCost = 0.7;
+inline double cta_cost(int steps, bool part) { return steps + kCtaCost + (part ? kPartCost : 0.0); }
+
+// The end of a launch under the block scheduler's rule: each block, in launch order, starts on
+// the SM that frees up first.
+double dispatch_end(const std::vector<double>& cost, int sms) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < sms; ++i) free_at.push(0.0);
+  double end = 0.0;
+  for (double c : cost) {
+    const double t = free_at.top() + c;
+    free_at.pop();
+    free_at.push(t);
+    end = std::max(end, t);
+  }
+  return end;
+}
+
+// Best-fit decreasing: items (costs in descending order) into `sms` SMs of capacity `cap`, each
+// into the fullest SM it still fits; false if one does not fit.
+bool best_fit(const std::vector<double>& cost, int sms, double cap, std::vector<int>& sm_of) {
+  std::multiset<std::pair<double, int>> load;
+  for (int i = 0; i < sms; ++i) load.insert({0.0, i});
+  for (size_t k = 0; k < cost.size(); ++k) {
+    auto it = load.upper_bound({cap - cost[k], INT_MAX});
+    if (it == load.begin()) return false;
+    --it;
+    const std::pair<double, int> e = *it;
+    load.erase(it);
+    sm_of[k] = e.second;
+    load.insert({e.first + cost[k], e.second});
+  }
+  return true;
+}
+
+int sm_count() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        v > 0)
+      return v;
+    cudaGetLastError();
+    return 152;
+  }();
+  return n;
+}
+
+// Full grid: each candidate cap c splits every key tile of more than c query tiles into parts of c
+// (the last one shorter); its CTAs are packed onto the SMs by best-fit decreasing at the smallest
+// capacity that holds them, and launched in the packing's planned start order. The plan with the
+// earliest end under the dispatch rule is taken if it beats the key-tile order by 2%.
+bool plan_full_grid(const int* tiles, int nkt, int G, int nbkv, int sms, BwdSplit& out) {
+  std::vector<double> base;
+  int most = 0;
+  for (int kt = 0; kt < nkt; ++kt) {
+    most = std::max(most, tiles[kt]);
+    for (int i = 0; i < nbkv; ++i) base.push_back(cta_cost(G * tiles[kt], false));
+  }
+  double best = 0.98 * dispatch_end(base, sms);
+  bool found = false;
+  struct Unit { int kt, part, nparts, t0, t1; };
+  std::vector<Unit> units;
+  std::vector<std::pair<double, int>> items;   // (cost, unit), one per CTA
+  std::vector<double> cost;
+  std::vector<int> sm_of, best_sm;
+  for (int cap = most - 1; cap >= std::max(1, most / 2); --cap) {
+    units.clear();
+    bool fits = true;
+    for (int kt = 0; kt < nkt && fits; ++kt) {
+      const int np = tiles[kt] > cap ? (tiles[kt] + cap - 1) / cap : 1;
+      if (np > kMaxParts) fits = false;
+      for (int q = 0; q < np; ++q) units.push_back({kt, q, np, q * cap, np > 1 ? std::min(tiles[kt], (q + 1) * cap) : 0});
+    }
+    if (!fits || (int)units.size() > kMaxUnits || (long long)units.size() * nbkv > kMaxCtas) continue;
+    items.clear();
+    for (int u = 0; u < (int)units.size(); ++u) {
+      const Unit& x = units[u];
+      const int steps = G * (x.nparts > 1 ? x.t1 - x.t0 : tiles[x.kt]);
+      for (int i = 0; i < nbkv; ++i) items.push_back({cta_cost(steps, x.nparts > 1), u});
+    }
+    std::stable_sort(items.begin(), items.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& b) {
+      return a.first > b.first;
+    });
+    cost.resize(items.size());
+    double total = 0.0;
+    for (size_t k = 0; k < items.size(); ++k) total += (cost[k] = items[k].first);
+    sm_of.assign(items.size(), 0);
+    double lo = std::max(total / sms, cost[0]), hi = dispatch_end(cost, sms) + 1.0;
+    if (!best_fit(cost, sms, hi, sm_of)) continue;
+    std::vector<int> fit = sm_of;
+    for (int it = 0; it < 24 && hi - lo > 0.05; ++it) {
+      const double mid = 0.5 * (lo + hi);
+      if (best_fit(cost, sms, mid, sm_of)) {
+        hi = mid;
+        fit = sm_of;
+      } else {
+        lo = mid;
+      }
+    }
+    // planned start of each CTA: on its SM, after the larger ones packed there before it
+    std::vector<double> start(items.size()), used(sms, 0.0);
+    for (size_t k = 0; k < items.size(); ++k) {
+      start[k] = used[fit[k]];
+      used[fit[k]] += cost[k];
+    }
+    std::vector<int> order(items.size());
+    for (size_t k = 0; k < order.size(); ++k) order[k] = (int)k;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+      return start[a] < start[b] || (start[a] == start[b] && fit[a] < fit[b]);
+    });
+    std::vector<double> ordered(order.size());
+    for (size_t k = 0; k < order.size(); ++k) ordered[k] = cost[order[k]];
+    const double end = dispatch_end(ordered, sms);
+    if (end >= best) continue;
+    best = end;
+    found = true;
+    // the plan: units (slots of the split tiles' parts in key-tile order), then the launch order
+    int slots = 0;
+    for (int u = 0; u < (int)units.size(); ++u) {
+      const Unit& x = units[u];
+      const uint32_t slot = x.nparts > 1 ? (uint32_t)slots++ : 0u;
+      out.units[u] = (uint32_t)x.kt | (uint32_t)x.part << 12 | (uint32_t)x.nparts << 16 | slot << 20;
+      out.range[u] = (uint32_t)x.t0 | (uint32_t)x.t1 << 16;
+    }
+    std::vector<int> next_bkv(units.size(), 0);
+    for (size_t k = 0; k < order.size(); ++k) {
+      const int u = items[order[k]].second;
+      out.ctas[k] = (uint32_t)u | (uint32_t)next_bkv[u]++ << 16;
+    }
+    out.n_units = (int)units.size();
+    out.n_slots = slots;
+    out.n_ctas = (int)order.size();
+  }
+  return found;
+}
+
+struct PlanKey {
+  int B, Hq, Hkv, Sq, Sk, causal, window, deterministic;
+  long long q_offset;
+  bool operator==(const PlanKey& o) const { return memcmp(this, &o, sizeof(PlanKey)) == 0; }
+};
+
+void plan_split_uncached(const Shape& s, BwdSplit& out) {
+  out.n_units = out.n_slots = out.n_ctas = 0;
   constexpr int BQ = 128;   // the query tile of both configurations
+  const int sms = sm_count();
   const int nkt = (s.Sk + kBN - 1) / kBN, G = s.Hq / s.Hkv;
   const long long nbkv = (long long)s.B * s.Hkv;
-  if (nkt > kMaxUnits || nkt > 4095) return;
-  // Only when one CTA per key tile leaves SMs idle: on a full GPU the heaviest-first key-tile order
-  // already balances the waves, and big parts pack worse. Never with deterministic dQ, whose turns
-  // need the key tiles dispatched in ascending order.
-  if (s.deterministic || (long long)nkt * nbkv >= kSms) return;
+  // Never with deterministic dQ, whose turns need the key tiles dispatched in ascending order.
+  if (s.deterministic || nkt > kMaxUnits || nkt > 4095 || nbkv > 0xffff) return;
   int tiles[kMaxUnits];
   long long total = 0, heaviest = 0;
   for (int kt = 0; kt < nkt; ++kt) {
@@ -977,9 +1126,14 @@ void plan_bwd_split(const Shape& s, BwdSplit& out) {
     total += (long long)G * tiles[kt];
     heaviest = std::max(heaviest, (long long)G * tiles[kt]);
   }
-  // the per-SM share of all steps; a key tile well above it is split into parts of about that size
-  const double share = (double)(total * nbkv) / kSms;
+  // the per-SM share of all steps
+  const double share = (double)(total * nbkv) / sms;
   if (share <= 0 || heaviest <= share) return;
+  if ((long long)nkt * nbkv >= sms) {
+    if ((long long)nkt * nbkv <= kMaxCtas) plan_full_grid(tiles, nkt, G, (int)nbkv, sms, out);
+    return;
+  }
+  // under-filled grid: key tiles above the share are cut into even parts of about that size
   int nparts[kMaxUnits];
   int units = 0, split = 0;
   for (int kt = 0; kt < nkt; ++kt) {
@@ -998,10 +1152,7 @@ void plan_bwd_split(const Shape& s, BwdSplit& out) {
   int slots = 0;
   for (int kt = 0; kt < nkt; ++kt) {
     slot_of[kt] = slots;
-    if (nparts[kt] > 1) {
-      out.split[out.n_split++] = (uint32_t)kt | (uint32_t)nparts[kt] << 12 | (uint32_t)slots << 16;
-      slots += nparts[kt];
-    }
+    if (nparts[kt] > 1) slots += nparts[kt];
   }
   if (slots >= 4096) return;
   struct U { double work; int kt, part; };
@@ -1012,12 +1163,73 @@ void plan_bwd_split(const Shape& s, BwdSplit& out) {
       list[n++] = U{(double)G * tiles[kt] / nparts[kt], kt, q};
   std::stable_sort(list, list + n, [](const U& a, const U& b) { return a.work > b.work; });
   for (int i = 0; i < n; ++i) {
-    const int kt = list[i].kt, q = list[i].part;
-    const uint32_t slot = nparts[kt] > 1 ? (uint32_t)(slot_of[kt] + q) : 0u;
-    out.units[i] = (uint32_t)kt | (uint32_t)q << 12 | (uint32_t)nparts[kt] << 16 | slot << 20;
+    const int kt = list[i].kt, q = list[i].part, np = nparts[kt];
+    const uint32_t slot = np > 1 ? (uint32_t)(slot_of[kt] + q) : 0u;
+    out.units[i] = (uint32_t)kt | (uint32_t)q << 12 | (uint32_t)np << 16 | slot << 20;
+    out.range[i] = (uint32_t)(q * tiles[kt] / np) | (uint32_t)((q + 1) * tiles[kt] / np) << 16;
   }
   out.n_units = n;
   out.n_slots = slots;
+}
+
+}  // namespace
+
+void plan_bwd_split(const Shape& s, BwdSplit& out) {
+  // the full-grid plan searches a few dozen packings: plans are kept for the last few shapes
+  constexpr int kCache = 4;
+  struct Entry { PlanKey key; BwdSplit plan; bool used; };
+  static thread_local Entry cache[kCache];
+  static thread_local int next = 0;
+  PlanKey key;
+  memset(&key, 0, sizeof(key));
+  key.B = s.B; key.Hq = s.Hq; key.Hkv = s.Hkv; key.Sq = s.Sq; key.Sk = s.Sk;
+  key.causal = s.causal; key.window = s.window; key.deterministic = s.deterministic; key.q_offset = s.q_offset;
+  for (Entry& e : cache)
+    if (e.used && e.key == key) {
+      out = e.plan;
+      return;
+    }
+  plan_split_uncached(s, out);
+  Entry& e = cache[next];
+  next = (next + 1) % kCache;
+  e.key = key;
+  e.plan = out;
+  e.used = true;
+}
+
+int bwd_plan_records(const Shape& s, int32_t* rec, int cap) {
+  static thread_local BwdSplit split;
+  plan_bwd_split(s, split);
+  const int nbkv = s.B * s.Hkv, nkt = (s.Sk + kBN - 1) / kBN;
+  const long long n = split.n_ctas > 0 ? split.n_ctas : (long long)nbkv * (split.n_units > 0 ? split.n_units : nkt);
+  for (long long i = 0; i < n && i < cap; ++i) {
+    int unit = (int)(i / nbkv), bkv = (int)(i % nbkv);
+    if (split.n_ctas > 0) {
+      unit = (int)(split.ctas[i] & 0xffffu);
+      bkv = (int)(split.ctas[i] >> 16);
+    }
+    int kt = unit, part = 0, nparts = 1;
+    if (split.n_units > 0) {
+      kt = (int)(split.units[unit] & 0xfffu);
+      part = (int)((split.units[unit] >> 12) & 0xfu);
+      nparts = (int)((split.units[unit] >> 16) & 0xfu);
+    }
+    int ib, ie;
+    key_tile_rows(s, kt, 128, ib, ie);
+    if (nparts > 1) {
+      const int base = ib;
+      ib = base + (int)(split.range[unit] & 0xffffu) * 128;
+      ie = std::min(ie, base + (int)(split.range[unit] >> 16) * 128);
+    }
+    int32_t* r = rec + 6 * i;
+    r[0] = kt;
+    r[1] = bkv;
+    r[2] = part;
+    r[3] = nparts;
+    r[4] = ib;
+    r[5] = ie;
+  }
+  return (int)n;
 }
 
 template <int D>
@@ -1053,7 +1265,16 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.tilemap = tm;
   }
   float* dsum = reinterpret_cast<float*>(ws + plan.dsum_off);
-  if ((e = launch_dsum(a, dsum, dq_acc, groups)) != cudaSuccess) return e;
+  static thread_local BwdSplit split;
+  plan_bwd_split(s, split);
+  int* part_sync = nullptr;
+  int n_sync = 0;
+  if (split.n_units > 0) {   // the split key tiles' counters start at zero, set by the D pass
+    part_sync = reinterpret_cast<int*>(ws + plan.cnt_off);
+    n_sync = (int)(plan.cnt_bytes / 4);
+  }
+  if ((e = launch_dsum(a, dsum, dq_acc, groups, reinterpret_cast<uint32_t*>(part_sync), n_sync)) != cudaSuccess)
+    return e;
   p.lse = a.lse;
   p.dsum = dsum;
   p.dq_acc = dq_acc;
@@ -1070,42 +1291,24 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
     p.turn = reinterpret_cast<int*>(ws + plan.turn_off);
     if ((e = cudaMemsetAsync(p.turn, 0, plan.turn_bytes, a.stream)) != cudaSuccess) return e;
   }
-  static thread_local BwdSplit split;
-  plan_bwd_split(s, split);
   p.n_units = split.n_units;
   p.n_slots = split.n_slots;
+  p.n_ctas = split.n_ctas;
   p.part = split.n_units > 0 ? reinterpret_cast<float*>(ws + plan.part_off) : nullptr;
+  p.part_sync = part_sync;
   memcpy(p.units, split.units, sizeof(uint32_t) * split.n_units);
+  memcpy(p.range, split.range, sizeof(uint32_t) * split.n_units);
+  memcpy(p.ctas, split.ctas, sizeof(uint32_t) * split.n_ctas);
   const int smem = C::BYTES;
   auto kernel = s.mask_kind != MK_NONE ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
-  const long long ctas = (long long)s.B * s.Hkv * (split.n_units > 0 ? split.n_units : p.nkt);
+  const long long ctas = split.n_ctas > 0 ? split.n_ctas : (long long)s.B * s.Hkv * (split.n_units > 0 ? split.n_units : p.nkt);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if ((e = prof_begin(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
   kernel<<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (split.n_units > 0) {
-    // the split key tiles' parts, summed in part order into dK / dV
-    static thread_local SplitReduceParams r;
-    r.s = s;
-    r.part = p.part;
-    r.dk = a.dk;
-    r.dv = a.dv;
-    r.accum = p.accum;
-    r.rows_begin = p.rows_begin;
-    r.n_rows = p.n_rows;
-    r.dk_rows = p.dk_rows;
-    r.dv_rows = p.dv_rows;
-    r.n_slots = split.n_slots;
-    r.n_split = split.n_split;
-    memcpy(r.split, split.split, sizeof(uint32_t) * split.n_split);
-    const long long threads = (long long)split.n_split * s.B * s.Hkv * kBN * (D / 4);
-    bwd_split_reduce_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(r);
-    count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   if ((e = prof_end(KID_BWD_MAIN, a.stream)) != cudaSuccess) return e;
   return launch_dq_convert(a, dq_acc, groups);
 }

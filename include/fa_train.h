@@ -310,6 +310,18 @@ FA_API fa_status fa_device_status(uint32_t* out);
  */
 FA_API fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream);
 
+/*
+ * The backward's work plan on the tensor-core path, for inspection (host only: no GPU work, no
+ * device needed). One record per CTA of the main kernel, in launch order, 6 int32 each: key tile
+ * (128 keys), batch * Hkv + key/value head, part, number of parts of that key tile (1: not split),
+ * and the query rows [first, end) the CTA walks (for every query head of the GQA group). A key
+ * tile cut into parts has its rows partitioned by them; the last part to finish sums the parts'
+ * fp32 partials in part order. Writes min(*n_ctas, cap) records to `records` (may be NULL when
+ * cap is 0) and the CTA count to *n_ctas. FA_ERR_UNSUPPORTED when the call would not take the
+ * tensor-core path.
+ */
+FA_API fa_status fa_train_bwd_plan(const fa_params* p, int32_t* records, int32_t cap, int32_t* n_ctas);
+
 /* Static description of a status code. */
 FA_API const char* fa_status_str(fa_status s);
 

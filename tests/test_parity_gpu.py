@@ -42,6 +42,10 @@ SMALL = [
     W("bf16_window_causal_accum", B=1, Hq=4, Hkv=1, Sq=300, Sk=1000, D=128, causal=True, q_offset=650,
       window=200, accum=True, seed=35),
     W("bf16_window_chunk_mid_d64", B=1, Hq=2, Hkv=2, Sq=200, Sk=900, D=64, q_offset=100, window=64, seed=36),
+    # a full grid whose first causal key tiles are cut in two and packed onto the SMs ahead of time
+    # (the part that finishes last sums the parts)
+    W("bf16_full_grid_planned_split", B=1, Hq=16, Hkv=16, Sq=1280, Sk=1280, D=128, causal=True, seed=37),
+    W("bf16_full_grid_planned_accum", B=2, Hq=8, Hkv=8, Sq=1280, Sk=1280, D=128, causal=True, accum=True, seed=38),
 ]
 
 
