@@ -49,7 +49,7 @@ constexpr int kRegsSoftmax = 208;
 static_assert((kRegsControl + 2 * kRegsSoftmax) * 128 <= kThreads * 168, "register split exceeds the launch pool");
 
 struct FwdTcParams {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   Shape s;
   const void* mask;
   const uint8_t* tilemap;   // [mask_batch, nqt, nkt] or null
@@ -431,14 +431,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     ok = __all_sync(0xffffffffu, ok);
     if (ok && idx > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], 0, abort_flag, p.status, 21));
     tc_fence_after();
-    if (ok) {
-      const bool row_ok = i < s.Sq;
-      const size_t row = (size_t)bh * s.Sq + (row_ok ? i : 0);
-      const bool alive = l > 0.f;
-      if (p.kv_splits == 1) {
+    const bool row_ok = i < s.Sq;
+    const size_t row = (size_t)bh * s.Sq + (row_ok ? i : 0);
+    const bool alive = l > 0.f;
+    if (p.kv_splits == 1) {
+      // The tile's O rows in bf16 go to its Q buffer, in the 128-byte-swizzled layout of the O
+      // tensor map, and leave in one TMA store per 64-column box (rows past Sq are clipped by the
+      // map). The buffer is free: the tile's last S MMAs completed before its last PV MMA (bar_o);
+      // with no visible key tile, once the Q load itself has landed.
+      if (ok) {
         const float inv = alive ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + head_base(s, b, h, s.Hq, s.Sq) +
-                                              (size_t)(row_ok ? i : 0) * row_stride(s, s.Hq));
+        if (idx == 0) mbar_wait(bar_q, 0, nullptr, p.status, 22);
+        const uint32_t sO = smem_u32(sQ + t * L::kTileBytes) + r * 128;
 #pragma unroll
         for (int cch = 0; cch < D / 32; ++cch) {
           uint32_t ov[32];
@@ -454,38 +458,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pkd[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (row_ok) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[cch * 4 + v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int c16 = (cch & 1) * 4 + v4;   // 16-byte chunk of the row inside its box
+            st_shared_v4(sO + (cch >> 1) * L::kBoxBytes + ((c16 ^ (r & 7)) << 4), pkd[4 * v4], pkd[4 * v4 + 1],
+                         pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
           }
         }
-        if (row_ok) p.lse[row] = alive ? (m + __log2f(l)) * kLn2 : 0.f;
-      } else {
-        const size_t rows = (size_t)s.B * s.Hq * s.Sq;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)split * rows + row) * D);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);   // all four warps of the warpgroup, whatever `ok` says
+      if (ok && wq == 0 && lane == 0 && q_row0 + t * kBM < s.Sq) {
+        for (int box = 0; box < D / 64; ++box)
+          tma_store_4d(&p.tm_o, sQ + t * L::kTileBytes + box * L::kBoxBytes, box * 64, q_row0 + t * kBM, h, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();   // the shared-memory source must outlive the reads
+      }
+      if (ok && row_ok) p.lse[row] = alive ? (m + __log2f(l)) * kLn2 : 0.f;
+    } else if (ok) {
+      const size_t rows = (size_t)s.B * s.Hq * s.Sq;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)split * rows + row) * D);
 #pragma unroll
-        for (int cch = 0; cch < D / 32; ++cch) {
-          uint32_t ov[32];
-          if (idx > 0) {
-            tmem_ld32(tO + cch * 32, ov);
-            tmem_wait_ld();
-            reg_fence(ov);
-          } else {
+      for (int cch = 0; cch < D / 32; ++cch) {
+        uint32_t ov[32];
+        if (idx > 0) {
+          tmem_ld32(tO + cch * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = 0u;
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[cch * 8 + v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
-                                              __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
-          }
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
         }
         if (row_ok) {
-          float2* ml = reinterpret_cast<float2*>(p.part_ml + ((size_t)split * rows + row) * 2);
-          *ml = make_float2(alive ? m : -CUDART_INF_F, l);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[cch * 8 + v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                            __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
         }
+      }
+      if (row_ok) {
+        float2* ml = reinterpret_cast<float2*>(p.part_ml + ((size_t)split * rows + row) * 2);
+        *ml = make_float2(alive ? m : -CUDART_INF_F, l);
       }
     }
   }
@@ -618,6 +631,7 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   if ((e = make_tmap_4d(&p.tm_q, a.q, s.layout, s.B, s.Hq, s.Sq, D, kBM)) != cudaSuccess) return e;
   if ((e = make_tmap_4d(&p.tm_k, a.k, kvl, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
   if ((e = make_tmap_4d(&p.tm_v, a.v, kvl, s.B, s.Hkv, s.Sk, D, kBN)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&p.tm_o, a.o, s.layout, s.B, s.Hq, s.Sq, D, kBM)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + kBM - 1) / kBM;
