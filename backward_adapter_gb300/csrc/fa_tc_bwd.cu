@@ -221,10 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = s.Hq / s.Hkv;
 
-  // ---- work unit: key tile kt of (b, kvh). Under the causal rule the low key tiles carry the most
-  //      work, so blocks run key-tile-major: every head's heavy tiles are in the first wave and the
-  //      light ones fill the SMs that free up (longest work first)
-  //      A split key tile's parts each take a consecutive share of its query tiles.
+  // ---- work unit: key tile kt of (b, kvh), or a part of it (consecutive query tiles). Without a
+  //      plan, blocks run key-tile-major: under the causal rule the low key tiles carry the most
+  //      work, so every head's heavy tiles are in the first wave and the light ones fill the SMs
+  //      that free up. With a plan (see plan_bwd_split) the host lists the units per block in the
+  //      order that packs them onto the SMs.
   const int nbkv = s.B * s.Hkv;
   int unit = blockIdx.x / nbkv, bkv = blockIdx.x % nbkv;
   if (p.n_ctas > 0) {   // the planned launch order
