@@ -46,6 +46,8 @@ SMALL = [
     # (the part that finishes last sums the parts)
     W("bf16_full_grid_planned_split", B=1, Hq=16, Hkv=16, Sq=1280, Sk=1280, D=128, causal=True, seed=37),
     W("bf16_full_grid_planned_accum", B=2, Hq=8, Hkv=8, Sq=1280, Sk=1280, D=128, causal=True, accum=True, seed=38),
+    W("bf16_full_grid_planned_bool_mask", B=2, Hq=8, Hkv=8, Sq=1280, Sk=1280, D=128, causal=True, mask="random_bool",
+      seed=39),
 ]
 
 

@@ -100,6 +100,11 @@ FUSED = [
                 mask="random_bool", accum=True, seed=62),
     wl.Workload("rows_f32_simt", B=1, Hq=2, Hkv=1, Sq=40, Sk=150, D=64, dtype="f32", causal=True, q_offset=110,
                 accum=True, seed=63),
+    # key tiles cut into parts: the part that finishes last writes the read-back rows
+    wl.Workload("rows_split_parts_d64", B=1, Hq=8, Hkv=2, Sq=768, Sk=1024, D=64, causal=True, q_offset=256,
+                accum=True, seed=64),
+    wl.Workload("rows_planned_full_grid", B=1, Hq=16, Hkv=16, Sq=1280, Sk=1280, D=128, causal=True, q_offset=0,
+                accum=True, seed=65),
 ]
 
 
