@@ -110,7 +110,7 @@ __device__ __forceinline__ bool skip_tile(const FwdTcParams& p, int mb, int qt0,
 }
 
 // MASKED: the call has a mask tensor (without one, the instance has no mixed-tile code).
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool POS_SCALE>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdTcParams p) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -287,6 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * D + lane_off;
     const float sl2 = s.scale * kLog2e;
+    // POS_SCALE (scale > 0): the scores stay unscaled in registers and the scale is folded into
+    // the exponent's FMA, one instruction per score fewer on a loop that is issue-bound; the tile
+    // max of the unscaled scores times sl2 is the max of the scaled ones. A scale of 0 or below
+    // takes the scaled copy (its max does not commute with the scaling).
+    const float inv_scale = POS_SCALE ? 1.f / s.scale : 0.f;
     // visible keys of this row: [key_lo, key_hi] from the causal rule and the window
     long long key_lo = 0, key_hi = (long long)s.Sk - 1;
     if (s.causal) key_hi = min(key_hi, s.q_offset + i);
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           // full, dead and partial tiles share one copy of the unrolled scaling (code size matters
           // here); a dead or partial tile then hides the keys outside [lo, lim] of this 32-key chunk
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c0 + e] = __uint_as_float(raw[e]) * sl2;
+          for (int e = 0; e < 32; ++e) x[c0 + e] = POS_SCALE ? __uint_as_float(raw[e]) : __uint_as_float(raw[e]) * sl2;
           if (!full) {
             const int a = max(lo - c0, 0), z = min(lim - c0 + 1, 32);
             const uint32_t vis = (dead || z <= a) ? 0u : (uint32_t)(((1ull << z) - 1ull) & ~((1ull << a) - 1ull));
@@ -348,7 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            x[c0 + e] = (mv[e] > kMaskFloor) ? fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e) : -CUDART_INF_F;
+            x[c0 + e] = (mv[e] > kMaskFloor) ? (POS_SCALE ? fmaf(mv[e], inv_scale, __uint_as_float(raw[e]))
+                                                          : fmaf(__uint_as_float(raw[e]), sl2, mv[e] * kLog2e))
+                                             : -CUDART_INF_F;
         } else {
           const uint8_t* mp = static_cast<const uint8_t*>(p.mask) + mrow + key0 + c0;
           uint32_t mb8[32];
@@ -365,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             for (int e = 0; e < 32; ++e) mb8[e] = (c0 + e >= lo && c0 + e <= lim) ? __ldg(mp + e) : 0u;
           }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c0 + e] = mb8[e] ? __uint_as_float(raw[e]) * sl2 : -CUDART_INF_F;
+          for (int e = 0; e < 32; ++e)
+            x[c0 + e] = mb8[e] ? (POS_SCALE ? __uint_as_float(raw[e]) : __uint_as_float(raw[e]) * sl2) : -CUDART_INF_F;
         }
       };
       // (TMEM loads and stores are warp-collective: every lane issues them, hidden rows just get -inf)
@@ -384,28 +392,38 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       }
       float tm4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};  // 4 independent chains
 #pragma unroll
-      for (int e = 0; e < kBN; ++e) tm4[e & 3] = fmaxf(tm4[e & 3], x[e]);
-      const float tmax = fmaxf(fmaxf(tm4[0], tm4[1]), fmaxf(tm4[2], tm4[3]));
+      for (int e = 0; e < kBN; e += 2) tm4[(e >> 1) & 3] = max3f(tm4[(e >> 1) & 3], x[e], x[e + 1]);
+      const float tmax_x = fmaxf(fmaxf(tm4[0], tm4[1]), fmaxf(tm4[2], tm4[3]));
+      const float tmax = (POS_SCALE && tmax_x != -CUDART_INF_F) ? tmax_x * sl2 : tmax_x;
       const float m_new = fmaxf(m, tmax);
       const bool rescale = m_new > m + kRescaleThreshold;   // false while nothing is visible
       const float m_use = rescale ? m_new : m;
       const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;
       const float m_sub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-      // P = 2^(x - m) as bf16 over the first 64 columns of the score block (all scores are in registers)
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(x - m) as bf16 over the first 64 columns of the score block (all scores are in registers);
+      // the exponent's FMA (or subtraction) and the row sum on packed fp32 pairs: this loop is
+      // issue-bound, and a pair instruction does the work of two
+      const uint64_t sl2_2 = f32x2(sl2, sl2), negm_2 = f32x2(-m_sub, -m_sub);
+      uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
       for (int cch = 0; cch < kBN / 32; ++cch) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(x[cch * 32 + 2 * e] - m_sub);
-          const float p1 = ex2_approx(x[cch * 32 + 2 * e + 1] - m_sub);
-          sum4[e & 3] += p0 + p1;
+          const uint64_t x2 = f32x2(x[cch * 32 + 2 * e], x[cch * 32 + 2 * e + 1]);
+          float t0, t1;
+          f32x2_split(POS_SCALE ? fma_f32x2(x2, sl2_2, negm_2) : add_f32x2(x2, negm_2), t0, t1);
+          const float p0 = ex2_approx(t0);
+          const float p1 = ex2_approx(t1);
+          sum2[e & 1] = add_f32x2(sum2[e & 1], f32x2(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + cch * 16, pk);
       }
-      const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      float s0, s1, s2, s3;
+      f32x2_split(sum2[0], s0, s1);
+      f32x2_split(sum2[1], s2, s3);
+      const float sum = (s0 + s1) + (s2 + s3);
       l = l * alpha + sum;
       m = m_use;
       if (__any_sync(0xffffffffu, rescale) && idx > 0) {  // alpha = 1 on rows that keep their max
@@ -650,7 +668,9 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   p.n_qpairs = n_qpairs(s);
   p.status = status;
   const int smem = FwdSmem<D>::kBytes;
-  auto kernel = s.mask_kind != MK_NONE ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  const bool pos = s.scale > 0.f;
+  auto kernel = s.mask_kind != MK_NONE ? (pos ? fwd_tc_kernel<D, true, true> : fwd_tc_kernel<D, true, false>)
+                                       : (pos ? fwd_tc_kernel<D, false, true> : fwd_tc_kernel<D, false, false>);
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const long long ctas = (long long)s.B * s.Hq * p.n_qpairs * plan.kv_splits;
