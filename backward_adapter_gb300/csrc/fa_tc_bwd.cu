@@ -100,7 +100,7 @@ struct BwdCfg {
   // fp32 dQ partial ([BQ][D] = 2 * Q_TILE bytes) until the reduce-add has read it
   static constexpr int OFF_STAGE = 2 * KV_TILE;
   static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * Q_TILE;   // [NDS] x dS^T (operand of the dQ MMA)
-  static constexpr int OFF_LSED = OFF_DS + NDS * DS_TILE;          // [NSTAGE] x (lse2[BQ], dsum[BQ])
+  static constexpr int OFF_LSED = OFF_DS + NDS * DS_TILE;          // [NSTAGE] x (-lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
   static constexpr int BYTES = OFF_BAR + 512;
   static_assert(RED_DQ || BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       for (int r = lane; r < BQ; r += 32) {
         const int i = it.i0 + r;
         const bool in = i < s.Sq;
-        dst[r] = in ? p.lse[rowbase + i] * l2e : 0.f;
+        dst[r] = in ? -(p.lse[rowbase + i] * l2e) : 0.f;   // negated: the exponent is one FMA
         dst[BQ + r] = in ? p.dsum[rowbase + i] : 0.f;
       }
       __syncwarp();
@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const int j = j0 + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = s.scale * kLog2e;
+    const uint64_t sl2_2 = f32x2(sl2, sl2);
     const bool key_ok = j < s.Sk;
     const size_t mrow0 = (size_t)mb * s.Sq;
     // query rows that see this key: [row_lo, row_hi] from the causal rule and the window
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tb = tmem + buf * C::BUF_COLS + lane_off;
-      const uint32_t lse_s = smem_u32(lsed + slot * 2 * BQ);  // [lse * log2(e) x BQ | D x BQ]
+      const uint32_t lse_s = smem_u32(lsed + slot * 2 * BQ);  // [-lse * log2(e) x BQ | D x BQ]
       const int code = bwd_tile_code(p, mb, it.i0, kt);
       // every pair of this step visible for this key: open tile, real key, all BQ rows inside the
       // key's row band (which also ends at the last real row)
@@ -548,8 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         uint32_t sr[32], dr[32];
         tmem_ld32(tb + c * 32, sr);
         if (cc > 0) tmem_ld32(tb + BQ + c * 32, dr);
-        // the chunk's 32 LSE values, loaded while the TMEM loads are in flight (the wait below
-        // orders every memory access, so loads issued after it would add their latency to it)
+        // the chunk's 32 (negated, log2-scaled) LSE values, loaded while the TMEM loads are in flight
+        // (the wait below orders every memory access, so loads issued after it would add their
+        // latency to it)
         float l2c[32];
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4) {
@@ -568,8 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             // full and partial tiles share the exponentials (one copy of the unrolled loop: code
             // size matters here); a partial tile then zeroes the query rows outside this key's
             // visible rows [rlo, rhi) (causal rule, window, query tail), a 16-bit set
+            // the exponents on packed fp32 pairs (this loop is issue-bound)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) pw[e] = ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, -l2[e]));
+            for (int e = 0; e < 16; e += 2) {
+              float t0, t1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[sub * 16 + e]), __uint_as_float(sr[sub * 16 + e + 1])),
+                                    sl2_2, f32x2(l2[e], l2[e + 1])),
+                          t0, t1);
+              pw[e] = ex2_approx(t0);
+              pw[e + 1] = ex2_approx(t1);
+            }
             if (!full) {
               const int base = it.i0 + q0;
               const int rlo = (int)max(0LL, min(row_lo - base, 16LL));
@@ -603,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 pw[e] = bias[e] != -CUDART_INF_F
-                            ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias[e] - l2[e]))
+                            ? ex2_approx(fmaf(__uint_as_float(sr[sub * 16 + e]), sl2, bias[e] + l2[e]))
                             : 0.f;
             }
           }
@@ -635,9 +645,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           const float* pw = pv + sub * 16;
           uint32_t dk8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dk8[e] = pack_bf16x2(pw[2 * e] * (__uint_as_float(dr[sub * 16 + 2 * e]) - dv_[2 * e]),
-                                 pw[2 * e + 1] * (__uint_as_float(dr[sub * 16 + 2 * e + 1]) - dv_[2 * e + 1]));
+          for (int e = 0; e < 8; ++e) {
+            // dS = P (dP - D) on packed fp32 pairs
+            float d0, d1;
+            f32x2_split(mul_f32x2(f32x2(pw[2 * e], pw[2 * e + 1]),
+                                  sub_f32x2(f32x2(__uint_as_float(dr[sub * 16 + 2 * e]),
+                                                  __uint_as_float(dr[sub * 16 + 2 * e + 1])),
+                                            f32x2(dv_[2 * e], dv_[2 * e + 1]))),
+                        d0, d1);
+            dk8[e] = pack_bf16x2(d0, d1);
+          }
           tmem_st8(tb + c * 32 + 16 + sub * 8, dk8);   // dS^T of these 16 queries
           // dS^T row of this key into the swizzled SMEM operand of the dQ MMA (2 x 16 B chunks)
 #pragma unroll
