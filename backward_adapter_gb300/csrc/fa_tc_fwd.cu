@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const uint32_t ph = (st / L::kStages) & 1;
         bool free_ok = true;
         for (; free_ok && released <= st - L::kStages; ++released)
-          free_ok = mbar_wait(&bar_s[1], released & 1, abort_flag, p.status, 1);
+          free_ok = mbar_wait<true>(&bar_s[1], released & 1, abort_flag, p.status, 1);
         if (!free_ok) break;
         mbar_arrive_expect_tx(&bar_full[sb], (prev >= 0 ? L::kTileBytes : 0) + (has_k ? L::kTileBytes : 0));
         for (int box = 0; box < D / 64; ++box) {
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         prev = j;
       }
       // Drain: every copy this thread issued has landed before the block can exit.
-      mbar_wait(bar_q, 0, nullptr, p.status, 2);
+      mbar_wait<true>(bar_q, 0, nullptr, p.status, 2);
       for (int i = 0; i < L::kStages; ++i)
-        if (used_mask >> i & 1u) mbar_wait(&bar_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 3);
+        if (used_mask >> i & 1u) mbar_wait<true>(&bar_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 3);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -238,18 +238,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           mma_ss(d_tmem, desc_add(dq0, off), desc_add(dk0, off), idesc_qk, k > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.status, 10);
+      bool ok = mbar_wait<true>(bar_q, 0, abort_flag, p.status, 10);
       tc_fence_after();
       int idx = 0;  // visible key tiles processed = ring stages consumed
       for (int j = kr.begin; ok && j < kr.end; ++j) {
         if (skip_tile(p, mb, qt0, j)) continue;
         const int sb = idx % L::kStages;
-        if (!(ok = mbar_wait(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 11))) break;
+        if (!(ok = mbar_wait<true>(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 11))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
           if (idx > 0) {
-            if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 12))) break;
+            if (!(ok = mbar_wait<true>(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 12))) break;
             tc_fence_after();
             issue_pv(t, 2 * sb + 1, idx - 1 > 0);
           }
@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       if (ok && idx > 0) {
         // the last stage holds only V of the last visible tile
         const int sb = idx % L::kStages;
-        ok = mbar_wait(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 15);
+        ok = mbar_wait<true>(&bar_full[sb], (idx / L::kStages) & 1, abort_flag, p.status, 15);
 #pragma unroll 1
         for (int t = 0; t < 2 && ok; ++t) {
-          if (!(ok = mbar_wait(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 14))) break;
+          if (!(ok = mbar_wait<true>(&bar_p[t], (idx - 1) & 1, abort_flag, p.status, 14))) break;
           tc_fence_after();
           issue_pv(t, 2 * sb + 1, idx - 1 > 0);
           mma_commit(&bar_o[t]);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       }
       // Every MMA this thread issued is complete before TMEM is released.
       mma_commit(bar_done);
-      mbar_wait(bar_done, 0, nullptr, p.status, 16);
+      mbar_wait<true>(bar_done, 0, nullptr, p.status, 16);
     }
    }
   } else {
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     bool ok = true;
     for (int j = kr.begin; j < kr.end; ++j) {
       if (skip_tile(p, mb, qt0, j)) continue;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], idx & 1, abort_flag, p.status, 20)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait<true>(&bar_s[t], idx & 1, abort_flag, p.status, 20)))) break;
       tc_fence_after();
       // scale into the log2 domain, then hide what the mask, the causal rule or the key tail hides
       const int code = tile_code(p, mb, qt0 + t, j);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     // ---- epilogue: O = acc / l, LSE = (m + log2 l) ln 2; a row with nothing visible gets 0 and 0
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && idx > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], 0, abort_flag, p.status, 21));
+    if (ok && idx > 0) ok = __all_sync(0xffffffffu, mbar_wait<true>(&bar_o[t], 0, abort_flag, p.status, 21));
     tc_fence_after();
     const bool row_ok = i < s.Sq;
     const size_t row = (size_t)bh * s.Sq + (row_ok ? i : 0);
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       // with no visible key tile, once the Q load itself has landed.
       if (ok) {
         const float inv = alive ? 1.f / l : 0.f;
-        if (idx == 0) mbar_wait(bar_q, 0, nullptr, p.status, 22);
+        if (idx == 0) mbar_wait<true>(bar_q, 0, nullptr, p.status, 22);
         const uint32_t sO = smem_u32(sQ + t * L::kTileBytes) + r * 128;
 #pragma unroll
         for (int cch = 0; cch < D / 32; ++cch) {

@@ -60,6 +60,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to 2 us inside the instruction until the phase
+// completes (a waiting warp then takes no issue slots from the warps sharing its SM sub-partition).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking probe: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -74,12 +86,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete. Returns false (and
 // records `site` in the error word and in *abort) if it does not complete
 // within the time limit, or if another role of the block has already aborted.
+// SLEEP: each probe may sleep up to 2 us in the instruction (better where the waiting warps share
+// their sub-partitions with issue-bound ones; the forward gains, the backward loses).
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status,
                                           unsigned site, unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort != nullptr && *abort) return false;
       if (globaltimer() - t0 > limit_ns) {
