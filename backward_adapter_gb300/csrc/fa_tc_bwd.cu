@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           idle_since = globaltimer();
         } else if (*abort_flag) {
           ok = false;
-        } else if ((__nanosleep(20), globaltimer() - idle_since > kWaitLimitNs)) {
+        } else if ((__nanosleep(80), globaltimer() - idle_since > kWaitLimitNs)) {
           *abort_flag = 1;
           atomicCAS(p.status, 0u, 0x80000000u | 111u);
           ok = false;
