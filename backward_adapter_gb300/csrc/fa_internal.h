@@ -182,6 +182,8 @@ bool tc_bwd_supported(const Shape& s);
 cudaError_t make_tmap_4d(struct CUtensorMap_st* map, const void* base, int layout, int B, int H, int S, int D,
                          int box_rows);
 cudaError_t make_tmap_f32_bhsd(struct CUtensorMap_st* map, const void* base, int S, int heads, int D, int box_rows);
+cudaError_t make_tmap_f32_bhsd_sw128(struct CUtensorMap_st* map, const void* base, int S, int heads, int D,
+                                     int box_rows);
 int tc_fwd_kv_splits(const Shape& s);
 cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);
 cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws);

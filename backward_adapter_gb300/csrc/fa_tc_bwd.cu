@@ -70,7 +70,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-  static constexpr bool RED_DQ = D == 128;              // dQ partial added from registers with red.add
+  static constexpr bool RED_DQ = false;                 // dQ partial added from registers with red.add
   static constexpr int BQ = 128;                        // query rows per step (N = 128 MMAs)
   static constexpr int NBUF = 1;                        // S/dP TMEM blocks
   static constexpr int BUF_COLS = 2 * BQ;               // block b: S^T [b*2BQ, +BQ), dP^T [b*2BQ+BQ, +BQ)
@@ -82,7 +82,7 @@ struct BwdCfg {
   static constexpr int DQ_COL = BQ;                     // dQ^T (D=128) / dQ (D=64) over the dP^T block
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
-  static constexpr bool DQ_TRANSPOSED = D == 128;      // dQ^T (lanes = d) vs dQ (lanes = query rows)
+  static constexpr bool DQ_TRANSPOSED = false;         // dQ^T (lanes = d) vs dQ (lanes = query rows)
   static constexpr int DQ_CHUNKS = (DQ_TRANSPOSED ? BQ : D) / 32;   // 32-column TMEM chunks of the dQ partial
   static constexpr int NSTAGE = 2;                      // Q/dO ring depth
   static constexpr int NDS = 1;                         // dS^T shared-memory buffers (the dQ MMA of a
@@ -916,17 +916,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
       } else {
         // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read:
-        // thread = query row, registers = features 32c + e; 16-byte chunks rotated across lanes
+        // thread = query row, registers = features 32c + e. Each 32-feature chunk c has its own
+        // [BQ][32] fp32 sub-tile with 128-byte rows, 128-byte swizzled (16-byte chunk u of row q
+        // at u ^ (q & 7)): conflict-free stores with static register indices, and the layout the
+        // reduce's tensor map reads
         static_assert(!C::DQ_TRANSPOSED, "the staged path takes dQ with query rows on TMEM lanes");
         const int q = wq * 32 + lane;
 #pragma unroll
         for (int c = 0; c < C::DQ_CHUNKS; ++c) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int cidx = (u + lane) & 7;
-            st_shared_v4(sbase + (q * D + c * 32 + 4 * cidx) * 4, v[c][4 * cidx], v[c][4 * cidx + 1],
-                         v[c][4 * cidx + 2], v[c][4 * cidx + 3]);
-          }
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(sbase + c * BQ * 128 + q * 128 + ((u ^ (q & 7)) << 4), v[c][4 * u], v[c][4 * u + 1],
+                         v[c][4 * u + 2], v[c][4 * u + 3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -945,7 +946,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             fence_proxy_async_global();
           }
           if (ok2) {
-            tma_reduce_add_3d(&p.tm_dq, sdq, 0, it.i0, (int)(group * bhq) + b * s.Hq + kvh * G + it.hh);
+            for (int c = 0; c < C::DQ_CHUNKS; ++c)
+              tma_reduce_add_3d(&p.tm_dq, reinterpret_cast<const uint8_t*>(sdq) + c * BQ * 128, c * 32, it.i0,
+                                (int)(group * bhq) + b * s.Hq + kvh * G + it.hh);
             bulk_commit_group();
             if (turn != nullptr) {
               // the whole add is complete and visible before the turn passes
@@ -1271,7 +1274,7 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   }
   float* dq_acc = reinterpret_cast<float*>(ws + plan.dqacc_off);
   const int groups = dq_groups(s);
-  if ((e = make_tmap_f32_bhsd(&p.tm_dq, dq_acc, s.Sq, groups * s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
+  if ((e = make_tmap_f32_bhsd_sw128(&p.tm_dq, dq_acc, s.Sq, groups * s.B * s.Hq, D, C::BQ)) != cudaSuccess) return e;
   p.s = s;
   p.mask = a.mask;
   p.nqt = (s.Sq + 127) / 128;

@@ -630,6 +630,21 @@ cudaError_t make_tmap_f32_bhsd(CUtensorMap* map, const void* base, int S, int he
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// fp32 [heads, S, D] tensor viewed as (D, S, heads), boxes of 32 x box_rows x 1 (128-byte rows) with
+// 128-byte swizzle: a 32-feature slice of a query tile, staged conflict-free in shared memory.
+cudaError_t make_tmap_f32_bhsd_sw128(CUtensorMap* map, const void* base, int S, int heads, int D, int box_rows) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)S * D * 4};
+  const cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_fwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq > 0; }
 
 int tc_fwd_kv_splits(const Shape& s) {
