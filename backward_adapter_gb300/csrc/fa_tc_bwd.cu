@@ -70,7 +70,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-  static constexpr bool RED_DQ = false;                 // dQ partial added from registers with red.add
   static constexpr int BQ = 128;                        // query rows per step (N = 128 MMAs)
   static constexpr int NBUF = 1;                        // S/dP TMEM blocks
   static constexpr int BUF_COLS = 2 * BQ;               // block b: S^T [b*2BQ, +BQ), dP^T [b*2BQ+BQ, +BQ)
@@ -79,11 +78,10 @@ struct BwdCfg {
   static constexpr bool TWO_ROUND = CHUNKS_PER_WARP == 2;   // the first 64 queries' dV / dK go early
   // chunk c of the scores (columns [32c, 32c+32)) is overwritten by P^T at [32c, 32c+16)
   // and dS^T at [32c+16, 32c+32) (bf16 pairs) once it has been read
-  static constexpr int DQ_COL = BQ;                     // dQ^T (D=128) / dQ (D=64) over the dP^T block
+  static constexpr int DQ_COL = BQ;                     // dQ (lanes = query rows) over the dP^T block
   static constexpr int DV_COL = 256;
   static constexpr int DK_COL = 256 + D;
-  static constexpr bool DQ_TRANSPOSED = false;         // dQ^T (lanes = d) vs dQ (lanes = query rows)
-  static constexpr int DQ_CHUNKS = (DQ_TRANSPOSED ? BQ : D) / 32;   // 32-column TMEM chunks of the dQ partial
+  static constexpr int DQ_CHUNKS = D / 32;             // 32-column TMEM chunks of the dQ partial
   static constexpr int NSTAGE = 2;                      // Q/dO ring depth
   static constexpr int NDS = 1;                         // dS^T shared-memory buffers (the dQ MMA of a
                                                         // step completes before the next dS^T is written)
@@ -103,7 +101,7 @@ struct BwdCfg {
   static constexpr int OFF_LSED = OFF_DS + NDS * DS_TILE;          // [NSTAGE] x (-lse2[BQ], dsum[BQ])
   static constexpr int OFF_BAR = OFF_LSED + NSTAGE * 2 * BQ * 4;
   static constexpr int BYTES = OFF_BAR + 512;
-  static_assert(RED_DQ || BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
+  static_assert(BQ * D * 4 <= 2 * Q_TILE, "dQ partial fits its stage slot");
   static_assert(NBUF * BUF_COLS + 2 * D <= 512, "TMEM columns");
   static_assert(BYTES <= 232448, "shared memory per block");
 };
@@ -298,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
       prefetch_tmap(&p.tm_do);
-      if (!C::RED_DQ) prefetch_tmap(&p.tm_dq);
+      prefetch_tmap(&p.tm_dq);
       if (!p.q8) {
         prefetch_tmap(&p.tm_k);
         prefetch_tmap(&p.tm_v);
@@ -308,26 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
           tma_load_4d(smem + C::OFF_V + box * C::KV_BOX, &p.tm_v, bar_kv, box * 64, j0, kvh, b);
         }
       }
-      // D = 128: the slot of step st is free once dK of step st - NSTAGE has read it, which the
-      // completion of that step's dQ MMA (issued after dK) implies; those completions of bar_dq_full
-      // are waited for one by one, in order, so its phase parity cannot alias. D = 64: the stager
-      // hands the slot back once the dQ partial staged in it has been reduced.
+      // the stager hands a slot back once the dQ partial staged in it has been reduced
       uint32_t used_mask = 0, phase_mask = 0;
-      int released = 0;
       StepIter it;
       it.init(G, iend, BQ, ibeg, s.deterministic != 0);
       for (int st = 0; it.valid(); it.next()) {
         if (step_skipped(it)) continue;
         const int slot = st % C::NSTAGE;
         const uint32_t ph = (st / C::NSTAGE) & 1;
-        bool free_ok = true;
-        if (C::RED_DQ) {
-          for (; free_ok && released <= st - C::NSTAGE; ++released)
-            free_ok = mbar_wait(&bar_dq_full[0], released & 1, abort_flag, p.status, 101);
-        } else {
-          free_ok = mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101);
-        }
-        if (!free_ok) break;
+        if (!mbar_wait(&bar_qdo_empty[slot], ph ^ 1, abort_flag, p.status, 101)) break;
         mbar_arrive_expect_tx(&bar_qdo_full[slot], 2 * C::Q_TILE);
         uint8_t* sq = smem + C::OFF_STAGE + slot * 2 * C::Q_TILE;
         const int qh = kvh * G + it.hh;   // query head
@@ -349,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, BQ, 0, 0);        // S^T, dP^T
       const uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);         // dV, dK (B = dO / Q, MN-major)
-      const uint32_t idesc_q = C::DQ_TRANSPOSED ? idesc_bf16_f32(128, BQ, 1, 1)   // dQ^T = K^T dS^T
-                                                : idesc_bf16_f32(128, D, 1, 1);   // dQ = dS K
+      const uint32_t idesc_q = idesc_bf16_f32(128, D, 1, 1);         // dQ = dS K
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       bool ok = mbar_wait(bar_kv, 0, abort_flag, p.status, 110);
       tc_fence_after();
@@ -414,12 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             smem_desc_sw128(smem_u32(smem + C::OFF_DS + (st % C::NDS) * C::DS_TILE), C::DS_BLOCK, 1024);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
-          if (C::DQ_TRANSPOSED)
-            mma_ss(tb + C::DQ_COL, desc_add(dKmn, k * 2048), desc_add(ds0, k * 2048), idesc_q, k > 0);
-          else
-            mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
+          mma_ss(tb + C::DQ_COL, desc_add(ds0, k * 2048), desc_add(dKmn, k * 2048), idesc_q, k > 0);
         }
-        mma_commit(&bar_dq_full[st % C::NBUF]);   // also frees the dS^T tile and, D = 128, the Q/dO slot
+        mma_commit(&bar_dq_full[st % C::NBUF]);   // also frees the dS^T tile
       };
 
       // Issue whichever MMA group is ready; none that waits holds back one that is ready. With one
@@ -839,14 +822,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // Deterministic dQ: the key tiles form groups of kDetGroup; each group has its own fp32 dQ
     // accumulator (summed in group order by the convert pass), and within a group the key tiles that
     // see a query tile add their partials to it in ascending key-tile order. A turn counter per
-    // (group, batch, query head, query tile) counts the passes: every stager warp (D = 128) or the
-    // leader thread (D = 64) of each earlier key tile adds one once its partial is added, steps the
-    // tile map skips included. The key tiles that see query tile i0 are the consecutive tiles from
-    // kt_first(i0) on, so a tile's rank in its group follows from the shape alone.
-    constexpr int kPassesPerCta = C::RED_DQ ? 4 : 1;
+    // (group, batch, query head, query tile) counts the passes: the leader thread of each earlier
+    // key tile adds one once its partial is added, steps the tile map skips included. The key tiles
+    // that see query tile i0 are the consecutive tiles from kt_first(i0) on, so a tile's rank in its
+    // group follows from the shape alone.
     const int group = s.deterministic ? kt / kDetGroup : 0;
     const size_t bhq = (size_t)s.B * s.Hq;
-    float* dq_acc_g = p.dq_acc + (size_t)group * bhq * s.Sq * D;
     auto turn_of = [&](const StepIter& t) -> int* {
       return p.turn + ((size_t)group * bhq + (size_t)(b * s.Hq + kvh * G + t.hh)) * p.nqt + t.i0 / 128;
     };
@@ -860,10 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (!s.deterministic) continue;
         // no partial from this key tile here, but its turn still passes
         int* turn = turn_of(it);
-        const bool mine = C::RED_DQ ? lane == 0 : leader;
         bool ok2 = true;
-        if (mine) {
-          ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 140);
+        if (leader) {
+          ok2 = wait_turn(turn, rank_of(it), abort_flag, p.status, 140);
           if (ok2) red_release_gpu_add(turn, 1);
         }
         if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
@@ -886,41 +866,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_dq_free[buf]);   // the TMEM block is free for the next dP^T
-      if constexpr (C::RED_DQ) {
-        // thread = feature d, registers = queries 32c + e: each warp instruction adds one 128-byte
-        // run of 32 consecutive features of one query row (rows past Sq are not touched)
-        const int d = wq * 32 + lane;
-        const int nrows = min(BQ, s.Sq - it.i0);
-        float* dst = dq_acc_g + ((size_t)(b * s.Hq + kvh * G + it.hh) * s.Sq + it.i0) * D + d;
-        int* turn = s.deterministic ? turn_of(it) : nullptr;
-        if (turn != nullptr) {
-          // this warp adds once the earlier key tiles of its group have passed (acquire by lane 0,
-          // then the whole warp)
-          bool ok2 = true;
-          if (lane == 0) ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 141);
-          if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
-          __syncwarp();
-          fence_acq_rel_gpu();
-        }
-#pragma unroll
-        for (int c = 0; c < C::DQ_CHUNKS; ++c) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < nrows) red_add_f32(dst + (size_t)(c * 32 + e) * D, __uint_as_float(v[c][e]));
-        }
-        if (turn != nullptr) {
-          // every lane's adds are performed before lane 0 passes the turn (release)
-          fence_acq_rel_gpu();
-          __syncwarp();
-          if (lane == 0) red_release_gpu_add(turn, 1);
-        }
-      } else {
+      {
         // then into the slot, whose Q and dO the dV / dK MMAs (issued before this dQ MMA) have read:
         // thread = query row, registers = features 32c + e. Each 32-feature chunk c has its own
         // [BQ][32] fp32 sub-tile with 128-byte rows, 128-byte swizzled (16-byte chunk u of row q
         // at u ^ (q & 7)): conflict-free stores with static register indices, and the layout the
         // reduce's tensor map reads
-        static_assert(!C::DQ_TRANSPOSED, "the staged path takes dQ with query rows on TMEM lanes");
         const int q = wq * 32 + lane;
 #pragma unroll
         for (int c = 0; c < C::DQ_CHUNKS; ++c) {
@@ -941,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (leader) {
           int* turn = s.deterministic ? turn_of(it) : nullptr;
           if (turn != nullptr) {
-            ok2 = wait_turn(turn, kPassesPerCta * rank_of(it), abort_flag, p.status, 142);
+            ok2 = wait_turn(turn, rank_of(it), abort_flag, p.status, 142);
             fence_acq_rel_gpu();
             fence_proxy_async_global();
           }
@@ -966,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       }
       ++st;
     }
-    if (!C::RED_DQ && leader) bulk_wait_group0();
+    if (leader) bulk_wait_group0();
   }
 
   tc_fence_before();

@@ -203,11 +203,6 @@ __device__ __forceinline__ bool wait_turn(const int* p, int target, volatile int
   }
 }
 
-// Fire-and-forget fp32 add into global memory (performed in L2).
-__device__ __forceinline__ void red_add_f32(float* ptr, float v) {
-  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
