@@ -115,11 +115,19 @@ cudaError_t prof_begin(int kid, cudaStream_t st);
 cudaError_t prof_end(int kid, cudaStream_t st);
 void count_launches(int n);
 
-// Deterministic dQ: the key tiles form groups of kDetGroup consecutive 128-key tiles; each group
+// Deterministic dQ: the key tiles form groups of det_group(s) consecutive 128-key tiles; each group
 // adds its partials in key-tile order into its own fp32 dQ accumulator, and the dQ convert pass
-// sums the groups' accumulators in group order. Without it there is one accumulator.
-constexpr int kDetGroup = 8;
-inline int dq_groups(const Shape& s) { return s.deterministic ? ((s.Sk + 127) / 128 + kDetGroup - 1) / kDetGroup : 1; }
+// sums the groups' accumulators in group order. Without it there is one accumulator. Every group
+// costs the D pass and the convert pass one more accumulator to zero and read; a longer group
+// chains more ordered adds per query tile. Groups of 32 (measured: causal S = 4096 step 0.737 ->
+// 0.658 ms against groups of 8) unless the keys far outnumber the query tiles, where every key
+// tile adds to the same few query tiles and the chains are the bound (the 67,584-key window over
+// 4 query tiles: 1.62 ms with groups of 8, 1.69 with 32).
+__host__ __device__ inline int det_group(const Shape& s) {
+  const int nkt = (s.Sk + 127) / 128, nqt = (s.Sq + 127) / 128;
+  return nkt <= 4 * nqt ? 32 : 8;
+}
+inline int dq_groups(const Shape& s) { return s.deterministic ? ((s.Sk + 127) / 128 + det_group(s) - 1) / det_group(s) : 1; }
 
 // Backward work split (tensor-core path). A key tile's query steps may be cut into up to kMaxParts
 // parts (consecutive query tiles), each a CTA of its own that writes fp32 dK/dV partials; the

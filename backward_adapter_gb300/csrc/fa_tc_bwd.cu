@@ -819,21 +819,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const bool leader = warp == 12 && lane == 0;
     StepIter it;
     it.init(G, iend, BQ, ibeg, s.deterministic != 0);
-    // Deterministic dQ: the key tiles form groups of kDetGroup; each group has its own fp32 dQ
+    // Deterministic dQ: the key tiles form groups of det_group(s); each group has its own fp32 dQ
     // accumulator (summed in group order by the convert pass), and within a group the key tiles that
     // see a query tile add their partials to it in ascending key-tile order. A turn counter per
     // (group, batch, query head, query tile) counts the passes: the leader thread of each earlier
     // key tile adds one once its partial is added, steps the tile map skips included. The key tiles
     // that see query tile i0 are the consecutive tiles from kt_first(i0) on, so a tile's rank in its
     // group follows from the shape alone.
-    const int group = s.deterministic ? kt / kDetGroup : 0;
+    const int det_g = det_group(s);
+    const int group = s.deterministic ? kt / det_g : 0;
     const size_t bhq = (size_t)s.B * s.Hq;
     auto turn_of = [&](const StepIter& t) -> int* {
       return p.turn + ((size_t)group * bhq + (size_t)(b * s.Hq + kvh * G + t.hh)) * p.nqt + t.i0 / 128;
     };
     auto rank_of = [&](const StepIter& t) -> int {
       const long long kt_first = s.window > 0 ? max(0LL, s.q_offset + t.i0 - s.window) / kBN : 0;
-      return kt - (int)max(kt_first, (long long)group * kDetGroup);
+      return kt - (int)max(kt_first, (long long)group * det_g);
     };
     int st = 0;
     for (; it.valid(); it.next()) {

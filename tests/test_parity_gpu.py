@@ -105,6 +105,11 @@ DETERMINISTIC = [
     W("det_causal_offset_accum_d64", B=1, Hq=4, Hkv=1, Sq=200, Sk=900, D=64, causal=True, q_offset=700,
       accum=True, seed=74),
     W("det_window_chunk_mid_d128", B=1, Hq=2, Hkv=1, Sq=300, Sk=1000, D=128, q_offset=200, window=150, seed=75),
+    # many more key tiles than query tiles: groups of 8 key tiles, two accumulators summed in order
+    W("det_long_keys_two_groups_of_8", B=1, Hq=4, Hkv=1, Sq=128, Sk=1500, D=128, causal=True, q_offset=1372,
+      seed=76),
+    # a causal square past 32 key tiles: two groups of 32
+    W("det_causal_two_groups_of_32", B=1, Hq=1, Hkv=1, Sq=4224, Sk=4224, D=64, causal=True, seed=77),
 ]
 
 
