@@ -16,7 +16,7 @@
 //                         dS^T = P^T (dP^T - D); P^T, dS^T -> TMEM (bf16), dS^T -> SMEM
 //     dV  += P^T dO          (TMEM x SMEM)
 //     dK  += dS^T Q          (TMEM x SMEM)
-//     dQ^T = K^T dS^T  (D = 128)  or  dQ = dS K  (D = 64)   (SMEM x SMEM -> TMEM)
+//     dQ  = dS K             (SMEM x SMEM -> TMEM)       query rows are TMEM lanes
 //     the dQ partial is added into the fp32 dQ accumulator in L2.
 // Roles: warp 0 TMA (K, V once; Q, dO per step), warp 1 MMA issue + TMEM owner,
 // warp 2 LSE/D staging, warps 4-11 softmax-grad: two warps per TMEM lane quadrant,
@@ -28,11 +28,10 @@
 // Each step's softmax-grad is split in two rounds of 64 queries; the first round's
 // dV / dK MMAs run while the second round is computed. S^T and dP^T complete on separate
 // barriers, so the first round's exponentials run under the dP^T MMAs.
-// D = 128: the dQ^T partial goes from TMEM to registers and into the accumulator with
-// coalesced red.add (one 128-byte run of 32 features per warp instruction), so it
-// needs no shared memory, and the Q/dO slot is handed back by the MMA commit after
-// dV / dK have read it. D = 64: the dQ partial is staged in the step's consumed Q/dO
-// slot and added with one TMA bulk tensor reduce-add.
+// The dQ partial is staged in the step's consumed Q/dO slot (128-byte swizzled 32-feature
+// sub-tiles) and added with TMA bulk tensor reduce-adds issued by one thread, which then hands
+// the slot back to the producer: per-element red.add from the stager warps took issue slots
+// from the softmax-grad warps sharing their sub-partitions.
 #include <cuda.h>
 #include <cstring>
 #include <cmath>
@@ -812,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     regs_inc<kRegsStager>();
     // ---------------------------------------------------------------- dQ stager (warps 12-15)
     // Each step's dQ partial leaves TMEM for the fp32 dQ accumulator, where the add happens in
-    // L2: D = 128 from registers with red.add, D = 64 through SMEM [BQ][D] and one TMA reduce-add
-    // issued by the leader thread.
+    // L2: through the step's consumed Q/dO slot and D/32 TMA reduce-adds issued by the leader
+    // thread.
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
