@@ -154,6 +154,9 @@ void plan_bwd_split(const Shape& s, BwdSplit& out);
 // The plan as records (see fa_train_bwd_plan): returns the CTA count, writes at most `cap` records.
 int bwd_plan_records(const Shape& s, int32_t* rec, int cap);
 
+// Streaming multiprocessors of the current device (queried once).
+int sm_count();
+
 FwdPlan plan_fwd(const Shape& s);
 BwdPlan plan_bwd(const Shape& s);
 

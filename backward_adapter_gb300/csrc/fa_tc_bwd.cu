@@ -974,18 +974,6 @@ bool best_fit(const std::vector<double>& cost, int sms, double cap, std::vector<
   return true;
 }
 
-int sm_count() {
-  static const int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        v > 0)
-      return v;
-    cudaGetLastError();
-    return 152;
-  }();
-  return n;
-}
-
 // Full grid: each candidate cap c splits every key tile of more than c query tiles into parts of c
 // (the last one shorter); its CTAs are packed onto the SMs by best-fit decreasing at the smallest
 // capacity that holds them, and launched in the packing's planned start order. The plan with the
@@ -1145,6 +1133,18 @@ void plan_split_uncached(const Shape& s, BwdSplit& out) {
 }
 
 }  // namespace
+
+int sm_count() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        v > 0)
+      return v;
+    cudaGetLastError();
+    return 152;
+  }();
+  return n;
+}
 
 void plan_bwd_split(const Shape& s, BwdSplit& out) {
   // the full-grid plan searches a few dozen packings: plans are kept for the last few shapes

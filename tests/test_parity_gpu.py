@@ -48,6 +48,15 @@ SMALL = [
     W("bf16_full_grid_planned_accum", B=2, Hq=8, Hkv=8, Sq=1280, Sk=1280, D=128, causal=True, accum=True, seed=38),
     W("bf16_full_grid_planned_bool_mask", B=2, Hq=8, Hkv=8, Sq=1280, Sk=1280, D=128, causal=True, mask="random_bool",
       seed=39),
+    # more 256-row query units than SMs: persistent forward CTAs chain several units each (the
+    # next unit's loads and first score MMAs overlapping the current one's epilogue)
+    W("bf16_persistent_causal_gqa_ragged", B=4, Hq=24, Hkv=6, Sq=500, Sk=500, D=128, causal=True, seed=40),
+    W("bf16_persistent_offset_d64", B=2, Hq=40, Hkv=8, Sq=300, Sk=700, D=64, causal=True, q_offset=400, seed=41),
+    W("bf16_persistent_window", B=2, Hq=48, Hkv=12, Sq=600, Sk=600, D=128, window=90, seed=42),
+    W("bf16_persistent_plain_accum_d64", B=3, Hq=32, Hkv=4, Sq=257, Sk=333, D=64, accum=True, seed=43),
+    # ... but not under a mask (its tile map may skip every key tile of a unit): one unit per CTA
+    W("bf16_many_units_bool_mask", B=2, Hq=24, Hkv=6, Sq=600, Sk=600, D=128, causal=True, mask="random_bool",
+      seed=44),
 ]
 
 
