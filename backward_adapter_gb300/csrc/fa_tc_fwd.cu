@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           }
         }
         fence_proxy_async_smem();
-        // all four warps of the warpgroup, whatever `ok` says; they leave with one verdict, so they
+        // all four warps of the warpgroup, whatever `ok` says; they leave with one shared answer, so they
         // run the same units and meet here equally often
         if constexpr (PERSIST)
           ok = named_bar_and(1 + t, 128, ok);
