@@ -527,6 +527,26 @@ fa_status fa_train_bwd_plan(const fa_params* p, int32_t* records, int32_t cap, i
   return FA_OK;
 }
 
+fa_status fa_train_fwd_plan(const fa_params* p, int32_t* ctas, int32_t* kv_splits, int32_t* persistent) {
+  Shape s;
+  fa_status st = check_params(p, s);
+  if (st != FA_OK) return st;
+  if (ctas == nullptr || kv_splits == nullptr || persistent == nullptr) {
+    set_error("ctas, kv_splits and persistent must be non-null");
+    return FA_ERR_INVALID_ARG;
+  }
+  const FwdPlan plan = plan_fwd(s);
+  if (!plan.tensor_core) {
+    set_error("this forward does not take the tensor-core path");
+    return FA_ERR_UNSUPPORTED;
+  }
+  const FwdLaunch l = tc_fwd_launch(s, plan.kv_splits);
+  *ctas = (int32_t)l.ctas;
+  *kv_splits = plan.kv_splits;
+  *persistent = l.persistent ? 1 : 0;
+  return FA_OK;
+}
+
 fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream) {
   if (limit_ms == 0 || limit_ms > 10000) {
     set_error("limit_ms=%u outside [1, 10000]", limit_ms);

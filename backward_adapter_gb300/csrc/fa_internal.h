@@ -196,6 +196,13 @@ cudaError_t make_tmap_f32_bhsd(struct CUtensorMap_st* map, const void* base, int
 cudaError_t make_tmap_f32_bhsd_sw128(struct CUtensorMap_st* map, const void* base, int S, int heads, int D,
                                      int box_rows);
 int tc_fwd_kv_splits(const Shape& s);
+// Launch shape of the tensor-core forward: CTAs and whether they are persistent (each chains the
+// key tiles of several 256-row units: more units than SMs, no mask, no key split).
+struct FwdLaunch {
+  long long ctas;
+  bool persistent;
+};
+FwdLaunch tc_fwd_launch(const Shape& s, int kv_splits);
 cudaError_t tc_fwd(const FwdArgs& a, const FwdPlan& plan, char* ws);
 cudaError_t tc_bwd(const BwdArgs& a, const BwdPlan& plan, char* ws);
 

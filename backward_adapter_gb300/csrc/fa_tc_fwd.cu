@@ -40,7 +40,6 @@ constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per tile
 constexpr int kRowsPerCta = 2 * kBM;
 constexpr int kThreads = 384;   // 12 warps
-constexpr int kNumSms = 152;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
@@ -828,10 +827,29 @@ bool tc_fwd_supported(const Shape& s) { return (s.D == 64 || s.D == 128) && s.Sq
 
 int tc_fwd_kv_splits(const Shape& s) {
   const long long units = (long long)s.B * s.Hq * n_qpairs(s);
-  if (units >= kNumSms) return 1;
-  const int by_waves = (int)((4LL * kNumSms) / units);
+  const int sms = sm_count();
+  if (units >= sms) return 1;
+  const int by_waves = (int)((4LL * sms) / units);
   const int by_len = kv_tiles_total(s) / 8;
   return max(1, min(by_waves, by_len));
+}
+
+FwdLaunch tc_fwd_launch(const Shape& s, int kv_splits) {
+  const long long units = (long long)s.B * s.Hq * n_qpairs(s);
+  // Persistent CTAs (more units than SMs) chain their units' key tiles, which needs a key tile in
+  // every unit: no split and no mask (whose tile map may skip all of a unit's tiles); a row sees at
+  // least its own diagonal key (q_offset + Sq <= Sk), so the range check below only guards that.
+  FwdLaunch l;
+  l.persistent = kv_splits == 1 && s.mask_kind == MK_NONE && units > sm_count();
+  FwdTcParams kp;
+  kp.s = s;
+  kp.kv_splits = 1;
+  for (int qp = 0; qp < n_qpairs(s) && l.persistent; ++qp) {
+    const KvRange kr = kv_range(kp, qp * kRowsPerCta, 0);
+    if (kr.end <= kr.begin) l.persistent = false;
+  }
+  l.ctas = l.persistent ? (long long)sm_count() : units * kv_splits;
+  return l;
 }
 
 template <int D>
@@ -861,15 +879,8 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
   p.part_ml = plan.kv_splits > 1 ? reinterpret_cast<float*>(ws + plan.part_ml_off) : nullptr;
   p.n_qpairs = n_qpairs(s);
   p.status = status;
-  const long long units = (long long)s.B * s.Hq * p.n_qpairs;
-  // Persistent CTAs (more units than SMs) chain their units' key tiles, which needs a key tile in
-  // every unit: no split and no mask (whose tile map may skip all of a unit's tiles); a row sees at
-  // least its own diagonal key (q_offset + Sq <= Sk), so the range check below only guards that.
-  bool persistent = plan.kv_splits == 1 && s.mask_kind == MK_NONE && units > sm_count();
-  for (int qp = 0; qp < p.n_qpairs && persistent; ++qp) {
-    const KvRange kr = kv_range(p, qp * kRowsPerCta, 0);
-    if (kr.end <= kr.begin) persistent = false;
-  }
+  const FwdLaunch launch = tc_fwd_launch(s, plan.kv_splits);
+  const bool persistent = launch.persistent;
   const int smem = FwdSmem<D>::kBytes;
   const bool pos = s.scale > 0.f;
   auto kernel = s.mask_kind != MK_NONE
@@ -878,7 +889,7 @@ static cudaError_t tc_fwd_t(const FwdArgs& a, const FwdPlan& plan, char* ws, uns
                                  : (pos ? fwd_tc_kernel<D, false, true, false> : fwd_tc_kernel<D, false, false, false>);
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
-  const long long ctas = persistent ? (long long)sm_count() : units * plan.kv_splits;
+  const long long ctas = launch.ctas;
   if ((e = prof_begin(KID_FWD, a.stream)) != cudaSuccess) return e;
   kernel<<<(unsigned)ctas, kThreads, smem, a.stream>>>(p);
   count_launches(1);

@@ -27,7 +27,7 @@ EXPORTED = ("fa_train_fwd_workspace_size", "fa_train_bwd_workspace_size", "fa_tr
             "fa_train_bwd_accum", "fa_status_str", "fa_last_error", "fa_profile_set_events",
             "fa_profile_launch_count", "fa_device_status", "fa_train_bwd_noalloc", "fa_train_selftest_wait",
             "fa_set_rows_backward", "fa_train_bwd_accum_rows", "fa_train_fwd_q8", "fa_train_bwd_q8",
-            "fa_train_bwd_accum_q8", "fa_train_bwd_plan")
+            "fa_train_bwd_accum_q8", "fa_train_bwd_plan", "fa_train_fwd_plan")
 FA_KERNEL_FWD, FA_KERNEL_BWD_MAIN, FA_KERNEL_BWD_DSUM, FA_KERNEL_BWD_DQ_CONVERT, FA_KERNEL_MASK_CLASSIFY = range(5)
 
 
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_train_bwd_accum_q8.restype = st
     lib.fa_train_bwd_plan.argtypes = [P, ctypes.POINTER(i32), i32, ctypes.POINTER(i32)]
     lib.fa_train_bwd_plan.restype = st
+    lib.fa_train_fwd_plan.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.fa_train_fwd_plan.restype = st
     _lib = lib
     return lib
 
@@ -204,6 +206,15 @@ def bwd_plan(p: FaParams) -> "list[tuple[int, int, int, int, int, int]]":
     rec = (ctypes.c_int32 * (6 * max(n.value, 1)))()
     _check(lib.fa_train_bwd_plan(ctypes.byref(p), rec, n.value, ctypes.byref(n)))
     return [tuple(rec[6 * i:6 * i + 6]) for i in range(n.value)]
+
+
+def fwd_plan(p: FaParams) -> "tuple[int, int, bool]":
+    """The forward's launch (host only): (CTAs, key splits per unit, persistent); see
+    fa_train_fwd_plan."""
+    lib = load_library()
+    ctas, splits, pers = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.fa_train_fwd_plan(ctypes.byref(p), ctypes.byref(ctas), ctypes.byref(splits), ctypes.byref(pers)))
+    return ctas.value, splits.value, bool(pers.value)
 
 
 def _on_device(t: torch.Tensor):

@@ -322,6 +322,19 @@ FA_API fa_status fa_train_selftest_wait(uint32_t limit_ms, void* stream);
  */
 FA_API fa_status fa_train_bwd_plan(const fa_params* p, int32_t* records, int32_t cap, int32_t* n_ctas);
 
+/*
+ * The forward's launch on the tensor-core path, for inspection (host only: no GPU work; without
+ * a device the SM count is taken as 152). A work unit is 256 query rows (two 128-row tiles) of
+ * one (batch, query head). Writes the main kernel's CTA count to *ctas, the key splits per unit
+ * to *kv_splits (> 1 when the units are fewer than the SMs and the keys are long enough: each CTA
+ * then takes one split, and a combine kernel merges the partial outputs), and 1 to *persistent
+ * when the CTAs are persistent (one per SM, each running several units in sequence: more units
+ * than SMs, no mask and no key split), else 0 (one unit, or one split of it, per CTA). All three
+ * pointers must be non-null. FA_ERR_UNSUPPORTED when the call would not take the tensor-core
+ * path (fp32, or D outside {64, 128}).
+ */
+FA_API fa_status fa_train_fwd_plan(const fa_params* p, int32_t* ctas, int32_t* kv_splits, int32_t* persistent);
+
 /* Static description of a status code. */
 FA_API const char* fa_status_str(fa_status s);
 
