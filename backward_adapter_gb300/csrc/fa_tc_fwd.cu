@@ -246,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // the previous unit's last V and the next unit's first K. A unit's Q tile t is loaded once
         // the previous unit's epilogue has drained its buffer (bar_qfree), after the boundary stage
         // whose V that epilogue waits for.
-        int st = 0, nq = 0;
+        int st = 0;
+        int nq[2] = {0, 0};   // Q loads issued per tile: the drain waits for the last of each
         int prev = -1, prev_kvh = 0, prev_b = 0;   // the stream's key tile whose V is still to load
         bool ok = true;
         auto stage = [&](bool has_k, int j, int kvh_k, int b_k) -> bool {
@@ -286,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             for (int box = 0; box < D / 64; ++box)
               tma_load_4d(sQ + t * L::kTileBytes + box * L::kBoxBytes, &p.tm_q, &bar_q[t], box * 64,
                           u.q_row0 + t * kBM, u.h, u.b);
+            nq[t] = ui + 1;
           }
-          nq = ui + 1;
           for (; ok; ++j) {
             while (j < u.kr.end && skip_tile(p, u.mb, u.qt0, j)) ++j;
             if (j >= u.kr.end) break;
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (ok && prev >= 0) stage(false, 0, 0, 0);   // the stream's last stage: V only
         // Drain: every copy this thread issued has landed before the block can exit.
         for (int t = 0; t < 2; ++t)
-          if (nq > 0) mbar_wait<true>(&bar_q[t], (nq - 1) & 1, nullptr, p.status, 2);
+          if (nq[t] > 0) mbar_wait<true>(&bar_q[t], (nq[t] - 1) & 1, nullptr, p.status, 2);
       }
       for (int i = 0; i < L::kStages; ++i)
         if (used_mask >> i & 1u) mbar_wait<true>(&bar_full[i], (phase_mask >> i) & 1u, nullptr, p.status, 3);
