@@ -890,28 +890,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (!__shfl_sync(0xffffffffu, filled ? 1 : 0, 0)) break;
         bool ok2 = true;
         if (leader) {
-          int* turn = s.deterministic ? turn_of(it) : nullptr;
-          if (turn != nullptr) {
-            ok2 = wait_turn(turn, rank_of(it), abort_flag, p.status, 142);
-            fence_acq_rel_gpu();
-            fence_proxy_async_global();
-          }
-          if (ok2) {
+          const int row_head = (int)(group * bhq) + b * s.Hq + kvh * G + it.hh;
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(sdq);
+          if (!s.deterministic) {
             for (int c = 0; c < C::DQ_CHUNKS; ++c)
-              tma_reduce_add_3d(&p.tm_dq, reinterpret_cast<const uint8_t*>(sdq) + c * BQ * 128, c * 32, it.i0,
-                                (int)(group * bhq) + b * s.Hq + kvh * G + it.hh);
+              tma_reduce_add_3d(&p.tm_dq, src + c * BQ * 128, c * 32, it.i0, row_head);
             bulk_commit_group();
-            if (turn != nullptr) {
-              // the whole add is complete and visible before the turn passes
+            bulk_wait_group_read0();
+          } else {
+            // in turn: the whole add is complete and visible before the turn passes
+            int* turn = turn_of(it);
+            ok2 = wait_turn(turn, rank_of(it), abort_flag, p.status, 142);
+            if (ok2) {
+              fence_acq_rel_gpu();
+              fence_proxy_async_global();
+              for (int c = 0; c < C::DQ_CHUNKS; ++c)
+                tma_reduce_add_3d(&p.tm_dq, src + c * BQ * 128, c * 32, it.i0, row_head);
+              bulk_commit_group();
               bulk_wait_group0();
               fence_proxy_async_global();
               fence_acq_rel_gpu();
               red_release_gpu_add(turn, 1);
-            } else {
-              bulk_wait_group_read0();
             }
-            mbar_arrive(&bar_qdo_empty[slot]);
           }
+          if (ok2) mbar_arrive(&bar_qdo_empty[slot]);
         }
         if (!__shfl_sync(0xffffffffu, ok2 ? 1 : 0, 0)) break;
       }
