@@ -183,7 +183,7 @@ __device__ __forceinline__ int bwd_tile_code(const BwdTcParams& p, int mb, int i
 // MASKED: the call has a mask tensor. Without one no tile is mixed, and that instance has no
 // mixed-tile code at all: the softmax-grad loop's unrolled variants compete for the instruction
 // cache with every other role's loop, and the unused one cost 3% of the causal backward.
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool DET>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   auto count_steps = [&]() {
     int n = 0;
     StepIter it;
-    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    it.init(G, iend, BQ, ibeg, DET);
     for (; it.valid(); it.next())
       if (!step_skipped(it)) ++n;
     return n;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       // the stager hands a slot back once the dQ partial staged in it has been reduced
       uint32_t used_mask = 0, phase_mask = 0;
       StepIter it;
-      it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+      it.init(G, iend, BQ, ibeg, DET);
       for (int st = 0; it.valid(); it.next()) {
         if (step_skipped(it)) continue;
         const int slot = st % C::NSTAGE;
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else if (warp == 2) {
     // ---------------------------------------------------------------- LSE / D staging
     StepIter it;
-    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    it.init(G, iend, BQ, ibeg, DET);
     const float l2e = kLog2e;
     for (int st = 0; it.valid(); it.next()) {
       if (step_skipped(it)) continue;
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(bar_kv);
     }
     StepIter it;
-    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    it.init(G, iend, BQ, ibeg, DET);
     int st = 0;
     bool ok = true;
     for (; it.valid(); it.next()) {
@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool leader = warp == 12 && lane == 0;
     StepIter it;
-    it.init(G, iend, BQ, ibeg, s.deterministic != 0);
+    it.init(G, iend, BQ, ibeg, DET);
     // Deterministic dQ: the key tiles form groups of det_group(s); each group has its own fp32 dQ
     // accumulator (summed in group order by the convert pass), and within a group the key tiles that
     // see a query tile add their partials to it in ascending key-tile order. A turn counter per
@@ -826,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // that see query tile i0 are the consecutive tiles from kt_first(i0) on, so a tile's rank in its
     // group follows from the shape alone.
     const int det_g = det_group(s);
-    const int group = s.deterministic ? kt / det_g : 0;
+    const int group = DET ? kt / det_g : 0;
     const size_t bhq = (size_t)s.B * s.Hq;
     auto turn_of = [&](const StepIter& t) -> int* {
       return p.turn + ((size_t)group * bhq + (size_t)(b * s.Hq + kvh * G + t.hh)) * p.nqt + t.i0 / 128;
@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     int st = 0;
     for (; it.valid(); it.next()) {
       if (step_skipped(it)) {
-        if (!s.deterministic) continue;
+        if (!DET) continue;
         // no partial from this key tile here, but its turn still passes
         int* turn = turn_of(it);
         bool ok2 = true;
@@ -892,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (leader) {
           const int row_head = (int)(group * bhq) + b * s.Hq + kvh * G + it.hh;
           const uint8_t* src = reinterpret_cast<const uint8_t*>(sdq);
-          if (!s.deterministic) {
+          if constexpr (!DET) {
             for (int c = 0; c < C::DQ_CHUNKS; ++c)
               tma_reduce_add_3d(&p.tm_dq, src + c * BQ * 128, c * 32, it.i0, row_head);
             bulk_commit_group();
@@ -1274,7 +1274,8 @@ static cudaError_t tc_bwd_t(const BwdArgs& a, const BwdPlan& plan, char* ws, uns
   memcpy(p.range, split.range, sizeof(uint32_t) * split.n_units);
   memcpy(p.ctas, split.ctas, sizeof(uint32_t) * split.n_ctas);
   const int smem = C::BYTES;
-  auto kernel = s.mask_kind != MK_NONE ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
+  auto kernel = s.mask_kind != MK_NONE ? (s.deterministic ? bwd_tc_kernel<D, true, true> : bwd_tc_kernel<D, true, false>)
+                                       : (s.deterministic ? bwd_tc_kernel<D, false, true> : bwd_tc_kernel<D, false, false>);
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const long long ctas = split.n_ctas > 0 ? split.n_ctas : (long long)s.B * s.Hkv * (split.n_units > 0 ? split.n_units : p.nkt);
