@@ -111,7 +111,7 @@ __device__ __forceinline__ bool fwd_unit(const FwdTcParams& p, int ui, FwdUnit& 
   const int BH = s.B * s.Hq;
   long long rest;
   int split = 0;
-  if (PERSIST) {
+  if constexpr (PERSIST) {
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     rest = (long long)ui * G + ((ui & 1) ? G - 1 - c : c);
     if (rest >= (long long)p.n_qpairs * BH) return false;
