@@ -654,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
           }
         }
         fence_proxy_async_smem();
-        // all four warps of the warpgroup, whatever `ok` says; they leave with one shared answer, so they
-        // run the same units and meet here equally often
+        // all four warps of the warpgroup, whatever `ok` says; in a persistent grid they leave with one
+        // shared answer, so they run the same units and meet here equally often
         if constexpr (PERSIST)
           ok = named_bar_and(1 + t, 128, ok);
         else
