@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       const bool row_ok = i < s.Sq;
       const size_t row = (size_t)u.bh * s.Sq + (row_ok ? i : 0);
       const bool alive = l > 0.f;
-      if (p.kv_splits == 1) {
+      if (PERSIST || p.kv_splits == 1) {   // a persistent grid never splits the keys
         // The tile's O rows in bf16 go to its Q buffer, in the 128-byte-swizzled layout of the O
         // tensor map, and leave in one TMA store per 64-column box (rows past Sq are clipped by the
         // map). The buffer is free: the tile's last S MMAs completed before its last PV MMA (bar_o);
